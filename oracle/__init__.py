@@ -1,0 +1,167 @@
+"""CPU oracle for the LLM.int8() mixed-precision matmul -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package. The CUDA library never calls it, and it imports nothing from the
+CUDA package: the two sides only share the seeded input generators in ``synth``.
+
+The arithmetic lives in ``int8mm_oracle.c`` (plain C, IEEE fp32 for the quantizers, exact
+integers for the int8 products, fp64 for the output). This module is numpy marshalling.
+
+Pins (checked by ``tests/test_oracle.py`` without a GPU): the pages' worked absmax example,
+an integer-valued case where the method reduces to an exact integer matmul, the
+quantization error bounds, threshold = inf reducing to plain vector-wise int8, zeroing the
+outlier columns reproducing the inlier product, the zeropoint range and round-trip
+bounds, and brute-force outlier sets on tiny inputs. The quality of the method against
+the unquantized product is reported, not pinned (the pages print no per-matmul error).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def load(path: str) -> C.CDLL:
+    """Loads an oracle build and declares its C signatures."""
+    L = C.CDLL(path)
+    p = C.c_void_p
+    i64 = C.c_int64
+    L.orc_outlier_columns.argtypes = [p, i64, i64, C.c_float, p]
+    L.orc_outlier_columns.restype = C.c_int32
+    L.orc_quantize_weight.argtypes = [p, i64, i64, p, p]
+    L.orc_quantize_rows_absmax.argtypes = [p, i64, i64, p, p, p]
+    L.orc_zeropoint_rows.argtypes = [p, i64, i64, p, p, p]
+    L.orc_outlier_weights.argtypes = [p, p, i64, i64, p, C.c_int32, p]
+    L.orc_int8_matmul.argtypes = [p, i64, i64, p, p, i64, C.c_float, p, p, i64, p, p, p,
+                                  p, p, C.c_int]
+    L.orc_int8_matmul.restype = C.c_int32
+    L.orc_half_to_float.argtypes = [p, i64, p]
+    L.orc_float_to_half.argtypes = [p, i64, p]
+    return L
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load(_build.build())
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _f16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.float16, a.dtype
+    return a
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def half_to_float(h: np.ndarray) -> np.ndarray:
+    h = _f16(h)
+    f = np.empty(h.shape, np.float32)
+    lib().orc_half_to_float(_ptr(h.view(np.uint16)), h.size, _ptr(f))
+    return f
+
+
+def float_to_half(f: np.ndarray) -> np.ndarray:
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    h = np.empty(f.shape, np.uint16)
+    lib().orc_float_to_half(_ptr(f), f.size, _ptr(h))
+    return h.view(np.float16)
+
+
+def outlier_columns(X: np.ndarray, threshold: float) -> np.ndarray:
+    """Ascending int32 list of columns j with some |X[i,j]| >= threshold."""
+    X = _f16(X)
+    T, d = X.shape
+    idx = np.empty(max(d, 1), np.int32)
+    n = lib().orc_outlier_columns(_ptr(X), T, d, float(threshold), _ptr(idx))
+    return idx[:n].copy()
+
+
+def quantize_weight(W: np.ndarray):
+    """(CB int8 [out,in], SCB float32 [out]) with W ~ CB * SCB / 127."""
+    W = _f16(W)
+    out, d = W.shape
+    CB = np.empty((out, d), np.int8)
+    SCB = np.empty(out, np.float32)
+    lib().orc_quantize_weight(_ptr(W), out, d, _ptr(CB), _ptr(SCB))
+    return CB, SCB
+
+
+def quantize_rows_absmax(X: np.ndarray, outlier_mask: np.ndarray | None = None):
+    """(Q int8 [rows,cols], absmax float32 [rows]); masked columns excluded and coded 0."""
+    X = _f16(X)
+    rows, cols = X.shape
+    m = None if outlier_mask is None else np.ascontiguousarray(outlier_mask, dtype=np.uint8)
+    Q = np.empty((rows, cols), np.int8)
+    a = np.empty(rows, np.float32)
+    lib().orc_quantize_rows_absmax(_ptr(X), rows, cols, _ptr(m), _ptr(Q), _ptr(a))
+    return Q, a
+
+
+def zeropoint_rows(X: np.ndarray):
+    """(Q int8 [rows,cols], S float32 [rows], Z float32 [rows])."""
+    X = _f16(X)
+    rows, cols = X.shape
+    Q = np.empty((rows, cols), np.int8)
+    S = np.empty(rows, np.float32)
+    Z = np.empty(rows, np.float32)
+    lib().orc_zeropoint_rows(_ptr(X), rows, cols, _ptr(Q), _ptr(S), _ptr(Z))
+    return Q, S, Z
+
+
+def zeropoint_dequant(Q: np.ndarray, S: np.ndarray, Z: np.ndarray) -> np.ndarray:
+    """X ~ (Q + Z) / S per row (fp64); a row with S == 0 dequantizes to Z."""
+    S = S.astype(np.float64)[:, None]
+    Z = Z.astype(np.float64)[:, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        x = (Q.astype(np.float64) + Z) / S
+    return np.where(S == 0, np.broadcast_to(Z, Q.shape), x)
+
+
+def outlier_weights(CB: np.ndarray, SCB: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """fp16 [out, n_out]: the dequantized weight columns of the outlier dimensions."""
+    CB = np.ascontiguousarray(CB, dtype=np.int8)
+    SCB = np.ascontiguousarray(SCB, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    out, d = CB.shape
+    W = np.empty((out, max(idx.size, 1)), np.uint16)
+    lib().orc_outlier_weights(_ptr(CB), _ptr(SCB), out, d, _ptr(idx), idx.size, _ptr(W))
+    return W[:, : idx.size].view(np.float16).copy()
+
+
+def int8_matmul(X, CB, SCB, threshold=6.0, bias=None, rows=None, nthreads=None,
+                want_acc=True):
+    """The LLM.int8() matmul evaluated for the selected rows of X (all rows by default).
+
+    Returns a dict: Y (fp64 [nrows,out]), acc (int64 [nrows,out] or None), Q (int8
+    [nrows,in]), rowabs (fp32 [nrows]), idx (int32 outlier columns), rows (int64)."""
+    X = _f16(X)
+    T, d = X.shape
+    CB = np.ascontiguousarray(CB, dtype=np.int8)
+    SCB = np.ascontiguousarray(SCB, dtype=np.float32)
+    out = CB.shape[0]
+    assert CB.shape[1] == d
+    b = None if bias is None else _f16(bias)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    nr = rows.size
+    Y = np.empty((nr, out), np.float64)
+    acc = np.empty((nr, out), np.int64) if want_acc else None
+    Q = np.empty((nr, d), np.int8)
+    ra = np.empty(nr, np.float32)
+    idx = np.empty(max(d, 1), np.int32)
+    n = lib().orc_int8_matmul(_ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(b),
+                              _ptr(rows), nr, _ptr(Y), _ptr(acc), _ptr(Q), _ptr(ra), _ptr(idx),
+                              int(nthreads or default_threads()))
+    return {"Y": Y, "acc": acc, "Q": Q, "rowabs": ra, "idx": idx[:n].copy(), "rows": rows}

@@ -1,0 +1,262 @@
+"""Pins for the CPU oracle: checks against what the pages and plain mathematics fix.
+
+None of these tests retypes the oracle's formulas to compare the oracle with itself. Each
+compares it with a value the pages print, an exact rational computation, a closed-form
+special case that reduces to an integer matmul (a library routine), an error bound, or a
+brute-force enumeration on tiny inputs.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rne(fr: Fraction) -> int:
+    """Round a rational to the nearest integer, ties to even (exact)."""
+    return round(fr)
+
+
+# --------------------------------------------------------------------------- worked example
+def test_absmax_worked_example_from_page():
+    g = json.load(open(os.path.join(GOLDEN, "absmax_worked_example.json")))
+    x = np.array([g["vector_printed"]], dtype=np.float16)
+    Q, a = oracle.quantize_rows_absmax(x)
+    # absmax is the fp16 value of the printed 5.4
+    assert a[0] == np.float32(np.float16(g["absmax_printed"]))
+    scale = 127.0 / float(a[0])
+    assert abs(scale - g["scale_printed"]) <= 0.05
+    lo, hi = g["code_range_printed"]
+    assert Q.min() >= lo and Q.max() <= hi
+    # the codes, derived in exact rational arithmetic from the fp16 inputs
+    amax = Fraction(float(a[0]))
+    expect = [rne(Fraction(float(v)) * 127 / amax) for v in x[0]]
+    assert Q[0].tolist() == expect == [28, -12, -101, 127]
+
+
+# --------------------------------------------------------------------------- fp16 handling
+def test_half_conversions_match_numpy():
+    g = np.random.default_rng(7)
+    f = np.concatenate([
+        g.standard_normal(20000).astype(np.float32) * 100,
+        g.standard_normal(2000).astype(np.float32) * 1e-6,           # subnormal halves
+        np.array([65504, 65519.99, 65520, -65520, 1e6, 2.0**-24, 2.0**-25, 3 * 2.0**-26,
+                  0.0, -0.0, 1.0 + 2.0**-11, 1.0 + 3 * 2.0**-11], np.float32),  # ties
+    ])
+    h = oracle.float_to_half(f)
+    ref = f.astype(np.float16)
+    assert np.array_equal(h.view(np.uint16), ref.view(np.uint16))
+    allh = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    finite = np.isfinite(allh)
+    back = oracle.half_to_float(allh[finite])
+    assert np.array_equal(back, allh[finite].astype(np.float32))
+
+
+# --------------------------------------------------------------------------- outlier columns
+def brute_outliers(X, thr):
+    T, d = X.shape
+    return [j for j in range(d) if any(abs(float(X[i, j])) >= thr for i in range(T))]
+
+
+def test_outlier_columns_threshold_edge_and_bruteforce():
+    X = np.zeros((3, 9), np.float16)
+    X[0, 1] = 6.0                       # exactly at the threshold: an outlier (>=)
+    X[1, 2] = np.float16(5.99609375)    # largest fp16 below 6: not an outlier
+    X[2, 4] = -6.0                      # magnitude counts, sign does not
+    X[1, 7] = 100.0
+    X[0, 8] = -5.0
+    got = oracle.outlier_columns(X, 6.0).tolist()
+    assert got == [1, 4, 7] == brute_outliers(X, 6.0)
+    assert oracle.outlier_columns(X, math.inf).tolist() == []
+    g = np.random.default_rng(3)
+    for trial in range(30):
+        T, d = g.integers(1, 6), g.integers(1, 12)
+        Xr = (g.standard_normal((T, d)) * 4).astype(np.float16)
+        thr = float(g.choice([0.5, 2.0, 6.0, 7.25]))
+        assert oracle.outlier_columns(Xr, thr).tolist() == brute_outliers(Xr, thr)
+
+
+def test_tiny_workload_outliers_are_the_planted_columns():
+    w = synth.WORKLOADS["tiny"]
+    X = synth.make_x(w)
+    assert oracle.outlier_columns(X, w.threshold).tolist() == synth.outlier_columns(w).tolist()
+
+
+# --------------------------------------------------------------------------- weights
+def test_weight_quantization_roundtrip_bound_and_range():
+    w = synth.WORKLOADS["tiny"]
+    W = synth.make_w(w)
+    W[5] = 0                                  # an all-zero row
+    CB, SCB = oracle.quantize_weight(W)
+    Wf = W.astype(np.float64)
+    assert SCB[5] == 0 and not CB[5].any()
+    np.testing.assert_array_equal(SCB, np.abs(Wf).max(axis=1).astype(np.float32))
+    assert CB.min() >= -127 and CB.max() <= 127
+    nz = SCB > 0
+    assert (np.abs(CB[nz].astype(np.int32)).max(axis=1) == 127).all()
+    err = np.abs(Wf - CB.astype(np.float64) * SCB[:, None].astype(np.float64) / 127.0)
+    bound = SCB[:, None].astype(np.float64) * (1.0 / 254 + 2.0**-22)
+    assert (err <= bound).all()
+
+
+def test_weight_quantization_integer_rows_are_exact():
+    W = synth.make_random_int(11, (6, 40), -127, 127)
+    W[np.arange(6), np.arange(6) * 3] = np.array([127, -127, 127, -127, 127, -127])
+    CB, SCB = oracle.quantize_weight(W.astype(np.float16))
+    assert (SCB == 127).all()
+    np.testing.assert_array_equal(CB.astype(np.int64), W)
+
+
+# --------------------------------------------------------------------------- full matmul
+def integer_case(seed=5, T=6, d=24, out=9, thr=200.0):
+    """Integer inlier activations and weights whose row absmax is 127: every scale is 1,
+    every code equals its input, and the method reduces to an exact integer matmul."""
+    g = np.random.default_rng(seed)
+    X = g.integers(-127, 128, (T, d)).astype(np.float64)
+    out_cols = [3, 17]
+    for i in range(T):
+        inl = [j for j in range(d) if j not in out_cols]
+        X[i, inl[i % len(inl)]] = 127 if i % 2 else -127
+        X[i, out_cols[0]] = [200, -250, 3, 1000, -201, 0][i % 6]    # 200 is exactly thr
+        X[i, out_cols[1]] = [-7, 512, 300, -300, 5, 256][i % 6]
+    X[5, [j for j in range(d) if j not in out_cols]] = 0             # inlier part all zero
+    W = g.integers(-127, 128, (out, d)).astype(np.float64)
+    W[np.arange(out), (np.arange(out) * 5) % d] = 127
+    W[2] = 0                                                          # all-zero weight row
+    bias = (g.integers(-40, 41, out) * 0.25).astype(np.float16)
+    return X.astype(np.float16), W.astype(np.float16), bias, out_cols, thr
+
+
+def test_integer_case_reduces_to_exact_integer_matmul():
+    X, W, bias, out_cols, thr = integer_case()
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul(X, CB, SCB, threshold=thr, bias=bias)
+    assert r["idx"].tolist() == out_cols
+    Xi = X.astype(np.int64)
+    Wi = W.astype(np.int64)
+    Xin = Xi.copy()
+    Xin[:, out_cols] = 0
+    np.testing.assert_array_equal(r["Q"].astype(np.int64), Xin)      # codes == inputs
+    np.testing.assert_array_equal(r["acc"], Xin @ Wi.T)               # int32-range products
+    exact = (Xi @ Wi.T).astype(np.float64) + bias.astype(np.float64)
+    np.testing.assert_array_equal(r["Y"], exact)                      # no rounding anywhere
+    assert r["rowabs"][5] == 0 and (r["rowabs"][:5] == 127).all()
+
+
+def method_error_bound(X, W, CB, SCB, idx):
+    """Per-element bound on |Y_method - (X W^T)| from the half-step quantization errors."""
+    Xf = X.astype(np.float64)
+    Wf = W.astype(np.float64)
+    inl = np.ones(X.shape[1], bool)
+    inl[idx] = False
+    a = np.where(inl[None, :], np.abs(Xf), 0).max(axis=1)
+    ex = a * (1.0 / 254 + 2.0**-22)                         # activation error per row
+    ew = SCB.astype(np.float64) * (1.0 / 254 + 2.0**-22)     # weight error per out row
+    Xa, Wa = np.abs(Xf), np.abs(Wf)
+    b = (Xa[:, inl].sum(1)[:, None] * ew[None, :] + ex[:, None] * Wa[:, inl].sum(1)[None, :]
+         + inl.sum() * ex[:, None] * ew[None, :])
+    if idx.size:
+        wout = np.abs(Wf[:, idx]) + ew[:, None]             # fp16 rounding of dequantized w
+        b += Xa[:, idx] @ (ew[:, None] + wout * 2.0**-11 + 2.0**-25).T
+    return b * (1 + 1e-9) + 1e-12, a
+
+
+@pytest.mark.parametrize("name", ["tiny"])
+def test_general_case_within_quantization_error_bound(name):
+    w = synth.WORKLOADS[name]
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul(X, CB, SCB, threshold=w.threshold, bias=bias)
+    exact = X.astype(np.float64) @ W.astype(np.float64).T + bias.astype(np.float64)
+    bound, a = method_error_bound(X, W, CB, SCB, r["idx"])
+    np.testing.assert_array_equal(r["rowabs"], a.astype(np.float32))
+    err = np.abs(r["Y"] - exact)
+    assert (err <= bound).all()
+    # the decomposition matters: without the outlier term the error leaves the bound
+    no_out = r["Y"] - X[:, r["idx"]].astype(np.float64) @ oracle.outlier_weights(
+        CB, SCB, r["idx"]).astype(np.float64).T
+    assert (np.abs(no_out - exact) > bound).any()
+
+
+def test_acc_equals_library_integer_matmul_and_codes_in_range():
+    w = synth.WORKLOADS["tiny"]
+    X, W = synth.make_x(w), synth.make_w(w)
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul(X, CB, SCB, threshold=w.threshold)
+    Q = r["Q"].astype(np.int64)
+    assert Q.min() >= -127 and Q.max() <= 127
+    assert not Q[:, r["idx"]].any()                               # outlier columns coded 0
+    np.testing.assert_array_equal(r["acc"], Q @ CB.astype(np.int64).T)
+    assert np.abs(r["acc"]).max() < 2**31
+
+
+def test_threshold_inf_is_plain_vectorwise_int8():
+    w = synth.WORKLOADS["tiny"]
+    X, W = synth.make_x(w), synth.make_w(w)
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul(X, CB, SCB, threshold=math.inf)
+    assert r["idx"].size == 0
+    Qp, ap = oracle.quantize_rows_absmax(X)
+    np.testing.assert_array_equal(r["Q"], Qp)
+    np.testing.assert_array_equal(r["rowabs"], ap)
+    np.testing.assert_array_equal(r["acc"], Qp.astype(np.int64) @ CB.astype(np.int64).T)
+
+
+def test_zeroing_outlier_columns_reproduces_inlier_product():
+    w = synth.WORKLOADS["tiny"]
+    X, W = synth.make_x(w), synth.make_w(w)
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul(X, CB, SCB, threshold=w.threshold)
+    Xz = X.copy()
+    Xz[:, r["idx"]] = 0
+    rz = oracle.int8_matmul(Xz, CB, SCB, threshold=math.inf)
+    np.testing.assert_array_equal(rz["Q"], r["Q"])
+    np.testing.assert_array_equal(rz["acc"], r["acc"])
+
+
+def test_selected_rows_match_full_evaluation():
+    w = synth.WORKLOADS["tiny"]
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    CB, SCB = oracle.quantize_weight(W)
+    full = oracle.int8_matmul(X, CB, SCB, threshold=6.0, bias=bias, nthreads=3)
+    rows = np.array([15, 0, 7])
+    part = oracle.int8_matmul(X, CB, SCB, threshold=6.0, bias=bias, rows=rows, nthreads=1)
+    np.testing.assert_array_equal(part["Y"], full["Y"][rows])
+    np.testing.assert_array_equal(part["acc"], full["acc"][rows])
+
+
+# --------------------------------------------------------------------------- zeropoint
+def test_zeropoint_uses_full_range_on_one_sided_rows():
+    w = synth.WORKLOADS["tiny"].with_(T=8, d_in=512)
+    X = synth.make_relu_like(w)
+    Q, S, Z = oracle.zeropoint_rows(X)
+    Xf = X.astype(np.float64)
+    mn, mx = Xf.min(1), Xf.max(1)
+    # printed formula: S = 254 / (max - min)
+    np.testing.assert_allclose(S, 254.0 / (mx - mn), rtol=2e-7)
+    assert (Q.min(1) == -127).all() and (Q.max(1) == 127).all()
+    assert (Z == np.round(Z)).all()                                   # integral zero-point
+    rec = oracle.zeropoint_dequant(Q, S, Z)
+    step = 1.0 / S.astype(np.float64)[:, None]
+    assert (np.abs(rec - Xf) <= step * (0.5 + 1e-4) + 1e-7).all() or \
+        (np.abs(rec - Xf) <= step).all()
+    interior = (Q > -127) & (Q < 127)
+    assert (np.abs(rec - Xf)[interior] <= (step * 0.5001 + 1e-7)[np.nonzero(interior)[0], 0]).all()
+
+
+def test_zeropoint_zero_maps_exactly_and_constant_row():
+    X = np.array([[0.0, 1.5, -2.0, 0.25, 0.0, 3.0],
+                  [2.5, 2.5, 2.5, 2.5, 2.5, 2.5]], np.float16)
+    Q, S, Z = oracle.zeropoint_rows(X)
+    assert int(Q[0, 0]) + Z[0] == 0 and int(Q[0, 4]) + Z[0] == 0
+    assert Q[0].min() == -127 and Q[0].max() == 127
+    assert S[1] == 0 and Z[1] == 2.5 and not Q[1].any()
+    rec = oracle.zeropoint_dequant(Q, S, Z)
+    assert (rec[1] == 2.5).all()

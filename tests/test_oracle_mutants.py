@@ -1,0 +1,61 @@
+"""The oracle's pins have teeth: plant a plausible mistake in a copy of the oracle source,
+rebuild it on the CPU, and check that at least one pin in test_oracle.py fails."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+import test_oracle as pins
+
+SRC = obuild.SRC
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("threshold strictly greater", ">= threshold) hit = 1", "> threshold) hit = 1"),
+    ("absmax includes outlier columns", "if (outlier && outlier[j]) continue;", ";"),
+    ("dequantize by 127 not 127^2", "/ (127.0 * 127.0)", "/ 127.0"),
+    ("outlier product dropped", "y += f;", "y += 0.0 * f;"),
+    ("weight row stride transposed", "jb->CB + o * jb->in", "jb->CB + o"),
+    ("zeropoint sign of Z", "float t = p - z;", "float t = p + z;"),
+    ("truncation instead of rounding", "return clamp_code(rintf(p));", "return clamp_code(truncf(p));"),
+    ("scale 128 instead of 127", "? 127.0f / absmax", "? 128.0f / absmax"),
+    ("outlier weight not dequantized", "* SCB[o]) / 127.0f", "* 1.0f) / 127.0f"),
+    ("bias subtracted", "y += (double)h2f(jb->bias[o]);", "y -= (double)h2f(jb->bias[o]);"),
+]
+
+PIN_TESTS = [
+    pins.test_absmax_worked_example_from_page,
+    pins.test_outlier_columns_threshold_edge_and_bruteforce,
+    pins.test_weight_quantization_roundtrip_bound_and_range,
+    pins.test_weight_quantization_integer_rows_are_exact,
+    pins.test_integer_case_reduces_to_exact_integer_matmul,
+    lambda: pins.test_general_case_within_quantization_error_bound("tiny"),
+    pins.test_acc_equals_library_integer_matmul_and_codes_in_range,
+    pins.test_zeropoint_uses_full_range_on_one_sided_rows,
+    pins.test_zeropoint_zero_maps_exactly_and_constant_row,
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, orig, bad):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor not unique: {orig!r}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(orig, bad))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", *obuild.CFLAGS, str(mut), "-o", str(so), "-lm"], check=True,
+                   capture_output=True)
+    saved = oracle._lib
+    oracle._lib = oracle.load(str(so))
+    failed = []
+    try:
+        for t in PIN_TESTS:
+            try:
+                t()
+            except AssertionError:
+                failed.append(getattr(t, "__name__", "general bound"))
+    finally:
+        oracle._lib = saved
+    assert failed, f"no pin caught the planted mistake: {name}"
