@@ -1,0 +1,157 @@
+/*
+ * int8mm -- LLM.int8() mixed-precision matrix multiply for NVIDIA B300 (sm_103a).
+ *
+ *   Y = dequant( int8(X_inlier) . int8(W)^T ) + X_outlier . W_outlier^T (fp16) + bias
+ *
+ * The method, as the source pages state it:
+ *   "Hugging Face, LLM.int8() 8-bit matrix multiplication integrated into Transformers
+ *    and Accelerate" (agentlenshq summary), section "core idea": (1) find hidden-state
+ *    columns holding a value of magnitude above a threshold (about 6); (2) multiply those
+ *    outlier columns in fp16 and quantize the rest to int8 vector-wise (activations per
+ *    row, weights per output feature); (3) dequantize the int8 product to fp16 and add the
+ *    fp16 outlier product. Section "zeropoint vs absmax": absmax scaling by 127/absmax.
+ *    Section "transformers integration": weights kept as int8 CB in [-127,127] with
+ *    W ~ (CB * SCB) / 127, quantized on the GPU when moved to it.
+ *   "LLM.int8() summary" (zenn, bilzard), section "method": the decomposition splits the
+ *    input dimensions and the matching weight dimensions; section "Zeropoint
+ *    Quantization": X8 = INT8(X16*S - Z), X16 = (X8 + Z)/S, S = 254/(max - min).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers to caller-owned memory; the library never
+ *     allocates or frees memory on these calls. Matrices are dense and row-major.
+ *   - fp16 tensors are passed as `void*` holding IEEE binary16 values.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call is
+ *     asynchronous on it and does not synchronize the host.
+ *   - Errors found on the host (arguments, alignment, device) are returned at once and
+ *     nothing is launched. Errors found on the device (outlier capacity exceeded, a wait
+ *     that timed out) are recorded in the workspace status word; read it with
+ *     i8_get_status(). No C++ exception crosses this interface.
+ *   - Every device pointer must be 16-byte aligned, else I8_ERR_ALIGNMENT.
+ *   - The device must be compute capability 10.3 (B300); there is no fallback.
+ *
+ * Rounding (fixed so that codes are reproducible bit for bit): absmax and absmax scale
+ * s = 127/absmax in IEEE fp32, code = rint(x*s) with one fp32 multiply (no fused
+ * multiply-add), round half to even, clamped to [-127,127]. An absmax of 0 gives scale 0
+ * and codes 0. Codes, outlier column sets and int32 accumulators are exact; Y is fp16.
+ */
+#ifndef INT8MM_H_
+#define INT8MM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  I8_OK = 0,
+  I8_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad threshold */
+  I8_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned, or `in` not a multiple of 16 */
+  I8_ERR_WORKSPACE = 3,          /* workspace null or smaller than required */
+  I8_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103 */
+  I8_ERR_CUDA = 5,               /* a CUDA runtime call failed (launch, tensor map, ...) */
+  I8_ERR_OUTLIER_CAP = 6,        /* device: more outlier columns than the workspace holds */
+  I8_ERR_TIMEOUT = 7             /* device: a pipeline wait gave up (kernel unwound safely) */
+} i8_status;
+
+/* Largest supported `in`: keeps |acc| <= 127*127*in below 2^31. */
+#define I8_MAX_IN 131072
+
+/*
+ * Vector-wise weight quantization ("core idea" step 2; "transformers integration":
+ * CB in [-127,127], W ~ CB*SCB/127, done once when the weight moves to the GPU).
+ *   W   : fp16 [out, in]            input
+ *   CB  : int8 [out, in]            output codes, CB[o,j] = rint(W[o,j] * 127/SCB[o])
+ *   SCB : fp32 [out]                output, SCB[o] = max_j |W[o,j]| (the absmax itself)
+ * out >= 0, in >= 0 (0 is a no-op). One kernel launch.
+ */
+i8_status int8_quantize_weight(const void* W, int out, int in, int8_t* CB, float* SCB,
+                               void* stream);
+
+/*
+ * Bytes of device workspace int8_matmul needs for these sizes. max_outlier_cols is the
+ * largest number of outlier columns the call must handle (<= 0 means `in`, the worst
+ * case); it is rounded up to a multiple of 64. Returns 0 for invalid sizes.
+ */
+size_t int8_matmul_workspace_size(int T, int in, int out, int max_outlier_cols);
+
+/*
+ * The LLM.int8() matmul (all three steps of "core idea").
+ *   X         : fp16 [T, in]       activations (hidden states), row-major
+ *   CB, SCB   : from int8_quantize_weight for W [out, in]
+ *   threshold : a column j is an outlier iff some |X[i,j]| >= threshold. +INF disables the
+ *               decomposition (plain vector-wise int8). NaN or <= 0: I8_ERR_INVALID_ARG.
+ *   bias      : fp16 [out] or NULL
+ *   Y         : fp16 [T, out]      output, Y = acc*rowabs_i*SCB_o/127^2 + outlier + bias
+ *   workspace : device buffer of ws_bytes >= int8_matmul_workspace_size(T,in,out,cap).
+ *               The outlier capacity used is the largest multiple of 64 columns that fits
+ *               in ws_bytes. Contents on entry are ignored. Two calls that run at the same
+ *               time must not share a workspace.
+ * `in` must be a multiple of 16 and <= I8_MAX_IN; T == 0 or out == 0 is a no-op.
+ * Launches: one memset of the workspace header and three kernels (column statistics,
+ * row quantize + outlier gather, tensor-core matmul). The outlier count stays on the
+ * device; no host synchronization.
+ */
+i8_status int8_matmul(const void* X, int T, int in, const int8_t* CB, const float* SCB, int out,
+                      float threshold, const void* bias, void* Y, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * int8_matmul plus copies of its intermediates, for tests. Each extra pointer may be NULL.
+ *   outlier_idx : int32 [in]       ascending outlier columns (first *n_out entries valid)
+ *   n_out       : int32 [1]        number of outlier columns
+ *   Xq          : int8 [T, in]     activation codes (outlier columns are 0)
+ *   rowabs      : fp32 [T]         per-row absmax over inlier columns
+ *   acc_s32     : int32 [T, out]   exact int8 product sum_j Xq[i,j]*CB[o,j]
+ */
+i8_status int8_matmul_debug(const void* X, int T, int in, const int8_t* CB, const float* SCB,
+                            int out, float threshold, const void* bias, void* Y,
+                            void* workspace, size_t ws_bytes, void* stream,
+                            int32_t* outlier_idx, int32_t* n_out, int8_t* Xq, float* rowabs,
+                            int32_t* acc_s32);
+
+/*
+ * Row-wise absmax quantization ("zeropoint vs absmax", absmax paragraph).
+ *   X      : fp16 [rows, cols]  input
+ *   Q      : int8 [rows, cols]  codes rint(x * 127/absmax)
+ *   absmax : fp32 [rows]        per-row max |x|
+ * One kernel launch.
+ */
+i8_status absmax_quantize_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
+                               void* stream);
+
+/*
+ * Row-wise zeropoint quantization ("Zeropoint Quantization": X8 = INT8(X*S - Z),
+ * S = 254/(max - min)). Z = rint(S*min) + 127 is an integer so that 0 maps to an exact
+ * code; dequantize with X ~ (Q + Z)/S. A constant row stores S = 0, Z = min, codes 0.
+ *   X : fp16 [rows, cols]; Q : int8 [rows, cols]; S, Z : fp32 [rows]. One kernel launch.
+ */
+i8_status zeropoint_quantize_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
+                                  float* Z, void* stream);
+
+/*
+ * Our own fp16 GEMM on the same tensor-core pipeline (no int8 step): the 16-bit
+ * comparator for the speed trade-off the pages discuss ("speed trade-off"; "INT8 speed").
+ *   X : fp16 [T, in]; W : fp16 [out, in]; bias : fp16 [out] or NULL; Y : fp16 [T, out]
+ *   Y = X . W^T + bias with fp32 accumulation. `in` a multiple of 16.
+ */
+i8_status f16_matmul(const void* X, int T, int in, const void* W, int out, const void* bias,
+                     void* Y, void* stream);
+
+/*
+ * Synchronizes `stream` and returns the device status word of the last int8_matmul that
+ * used this workspace (I8_OK, I8_ERR_OUTLIER_CAP or I8_ERR_TIMEOUT).
+ */
+i8_status i8_get_status(const void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* i8_status_string(i8_status s);
+
+/* Number of kernels (and memsets) the last successful call on this host thread launched. */
+int i8_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INT8MM_H_ */

@@ -1,0 +1,92 @@
+// Internal declarations shared by the kernel translation units and the C-ABI layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/int8mm.h"
+
+namespace i8mm {
+
+constexpr int kSmCount = 148;       // B300: 2 dies x 74 SMs
+constexpr int kKBlock = 64;         // K elements per pipeline stage (128 bytes of fp16)
+constexpr int kChunkKBlocks = 16;   // K blocks per exact fp32 accumulation chunk (1024 K)
+
+// Device status header at the start of every int8_matmul workspace (zeroed per call).
+struct WsHeader {
+  int32_t status;         // first device-side error (i8_status), 0 if none
+  uint32_t arrive;        // CTA arrival counter of the column-statistics pass
+  int32_t n_out;          // number of outlier columns found
+  int32_t n_out_used;     // min(n_out, capacity): columns actually gathered
+  int32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
+
+// Byte offsets of the int8_matmul workspace sections. Computed identically by
+// int8_matmul_workspace_size() and int8_matmul().
+struct WsLayout {
+  size_t header = 0, mask = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0, total = 0;
+  size_t zero_bytes = 0;  // header + mask: memset at the start of every call
+  int words = 0;          // 32-column words of the outlier mask
+  int ncap = 0;           // outlier column capacity (multiple of 64)
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int T, int in, int out, int ncap) {
+  WsLayout L;
+  size_t off = 0;
+  L.words = (in + 31) / 32;
+  L.ncap = ncap;
+  L.header = off; off += sizeof(WsHeader);
+  L.mask = off; off = align_up(off + sizeof(uint32_t) * L.words, 256);
+  L.zero_bytes = off;
+  L.idx = off; off = align_up(off + sizeof(int32_t) * (size_t)in, 256);
+  L.xq = off; off = align_up(off + 2 * (size_t)T * in, 256);
+  L.rowabs = off; off = align_up(off + 4 * (size_t)T, 256);
+  L.xout = off; off = align_up(off + 2 * (size_t)T * ncap, 256);
+  L.wout = off; off = align_up(off + 2 * (size_t)out * ncap, 256);
+  L.total = off;
+  return L;
+}
+
+// Smallest fp16 bit pattern whose value is >= threshold (0x7C00 = +inf if none is finite).
+uint16_t threshold_to_half_bits(float threshold);
+
+// ---- kernel launchers (each returns cudaGetLastError() of its launch)
+cudaError_t launch_colstats(const void* X, int T, int in, uint16_t thr_bits, WsHeader* hdr,
+                            uint32_t* mask, int32_t* idx, int ncap, cudaStream_t s);
+cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* CB,
+                                   const float* SCB, int out, const WsHeader* hdr,
+                                   const uint32_t* mask, const int32_t* idx, int ncap,
+                                   void* xq16, float* rowabs, void* xout, void* wout,
+                                   int8_t* xq8_debug, cudaStream_t s);
+cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
+                               cudaStream_t s);
+cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
+                                  float* Z, cudaStream_t s);
+
+struct GemmArgs {
+  // A operand (M side = output features): int8 CB [out, in] converted in-kernel, or an
+  // fp16 weight [out, in] loaded directly (the fp16 comparator).
+  const void* a_int8 = nullptr;
+  const void* a_f16 = nullptr;
+  // B operand (N side = tokens): fp16 [T, in] (activation codes, or raw X for fp16)
+  const void* b_f16 = nullptr;
+  // Outlier slices (fp16): W_out [out, ncap] and X_out [T, ncap]; n_out read on device
+  const void* wout = nullptr;
+  const void* xout = nullptr;
+  int ncap = 0;
+  WsHeader* hdr = nullptr;      // status word + n_out (int8 path), may be null for fp16
+  const float* rowabs = nullptr;
+  const float* scb = nullptr;
+  const void* bias = nullptr;
+  void* Y = nullptr;
+  int32_t* acc_debug = nullptr; // optional [T, out] int32 export
+  int T = 0, in = 0, out = 0;
+  uint64_t timeout_ns = 2000000000ull;
+  int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+}  // namespace i8mm

@@ -1,0 +1,253 @@
+// Row quantizers: vector-wise absmax (activations and weights), the fused activation
+// quantize + outlier gather of the matmul, and zeropoint rows.
+//
+// "Hugging Face, LLM.int8() ... Transformers and Accelerate" (agentlenshq):
+//   section "core idea", step 2: the non-outlier part is quantized to int8 vector-wise
+//     (activations per row, weights per output feature) and the outlier part stays fp16;
+//   section "zeropoint vs absmax": absmax scaling, divide by absmax and multiply by 127;
+//   section "transformers integration": CB in [-127,127], W ~ (CB * SCB) / 127.
+// "LLM.int8() summary" (zenn), section "Zeropoint Quantization":
+//   X8 = INT8(X16*S - Z), X16 = (X8 + Z)/S, S = 254/(max - min).
+//
+// Every rounding step uses an explicit IEEE intrinsic (__fdiv_rn, __fmul_rn, __fsub_rn,
+// __float2int_rn), so the codes do not depend on contraction flags:
+//   s = 127/absmax (0 if absmax is 0), code = clamp(rint(x*s), -127, 127).
+// One CTA of 256 threads quantizes one row; rows are read with 16-byte loads when the
+// row length is a multiple of 8 elements, element by element otherwise.
+#include "int8mm_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace i8mm {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ int absmax_code(float x, float s) {
+  int q = __float2int_rn(__fmul_rn(x, s));
+  return max(-127, min(127, q));
+}
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// Block-wide max of non-negative values held as unsigned bit patterns.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* s_red) {
+  v = __reduce_max_sync(0xffffffffu, v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  uint32_t r = 0;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) r = max(r, s_red[w]);
+  __syncthreads();
+  return r;
+}
+
+// Masked-column test: bit j of the mask words flags column j as an outlier.
+__device__ __forceinline__ bool is_masked(const uint32_t* smask, int j) {
+  return (smask[j >> 5] >> (j & 31)) & 1u;
+}
+
+// Quantizes one row of `cols` fp16 values.
+//   kMasked: columns flagged in smask are excluded from the absmax and coded 0.
+//   q8 (nullable): int8 codes; q16 (nullable): the same codes as exact fp16 values.
+// Returns the row absmax (over unmasked columns).
+template <bool kMasked>
+__device__ float quantize_row(const uint16_t* __restrict__ x, int cols,
+                              const uint32_t* smask, int8_t* __restrict__ q8,
+                              uint16_t* __restrict__ q16, uint32_t* s_red) {
+  const int tid = threadIdx.x;
+  const bool vec = (cols & 7) == 0;
+  uint32_t mx = 0;  // running max of |x| bit patterns
+  if (vec) {
+    const int nch = cols >> 3;
+    for (int c = tid; c < nch; c += kRowThreads) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + c);
+      uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                       v.w & 0x7fff7fffu};
+      if (kMasked) {
+        const uint32_t mb = (smask[c >> 2] >> ((c & 3) * 8)) & 0xffu;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t keep = ((mb >> (2 * k)) & 1u ? 0u : 0x0000ffffu) |
+                                ((mb >> (2 * k + 1)) & 1u ? 0u : 0xffff0000u);
+          w[k] &= keep;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+    }
+  } else {
+    for (int j = tid; j < cols; j += kRowThreads) {
+      if (kMasked && is_masked(smask, j)) continue;
+      mx = max(mx, (uint32_t)(x[j] & 0x7fffu));
+    }
+  }
+  const float a = h2f((uint16_t)block_max_u32(mx, s_red));
+  const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
+
+  if (vec) {
+    const int nch = cols >> 3;
+    for (int c = tid; c < nch; c += kRowThreads) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t mb = kMasked ? (smask[c >> 2] >> ((c & 3) * 8)) & 0xffu : 0u;
+      int q[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        q[2 * k] = absmax_code(h2f(w[k] & 0xffffu), s);
+        q[2 * k + 1] = absmax_code(h2f(w[k] >> 16), s);
+      }
+      if (kMasked) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if ((mb >> e) & 1u) q[e] = 0;
+      }
+      if (q8) {
+        uint2 o;
+        o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
+              ((uint32_t)(q[3] & 0xff) << 24);
+        o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
+              ((uint32_t)(q[7] & 0xff) << 24);
+        reinterpret_cast<uint2*>(q8)[c] = o;
+      }
+      if (q16) {
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          ow[k] = (uint32_t)__half_as_ushort(__int2half_rn(q[2 * k])) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(q[2 * k + 1])) << 16);
+        reinterpret_cast<uint4*>(q16)[c] = o;
+      }
+    }
+  } else {
+    for (int j = tid; j < cols; j += kRowThreads) {
+      int q = absmax_code(h2f(x[j]), s);
+      if (kMasked && is_masked(smask, j)) q = 0;
+      if (q8) q8[j] = (int8_t)q;
+      if (q16) q16[j] = __half_as_ushort(__int2half_rn(q));
+    }
+  }
+  return a;
+}
+
+// Standalone absmax rows; also the weight quantizer (rows = output features).
+__global__ void __launch_bounds__(kRowThreads) absmax_rows_kernel(
+    const uint16_t* __restrict__ X, int cols, int8_t* __restrict__ Q, float* __restrict__ amax) {
+  __shared__ uint32_t s_red[kRowThreads / 32];
+  const size_t row = blockIdx.x;
+  const float a = quantize_row<false>(X + row * cols, cols, nullptr, Q + row * cols, nullptr,
+                                      s_red);
+  if (threadIdx.x == 0) amax[row] = a;
+}
+
+// Fused activation quantize + outlier gather of the matmul.
+//   blocks [0, T): row i -> fp16 codes (outlier columns 0), rowabs[i], and
+//                  X_out[i, k] = X[i, idx[k]] for k < n, zeros up to a multiple of 64;
+//   blocks [T, ..): 32 output features each -> W_out[o, k] = fp16((CB[o,idx[k]]*SCB[o])/127).
+__global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
+    const uint16_t* __restrict__ X, int T, int in, const int8_t* __restrict__ CB,
+    const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
+    const uint32_t* __restrict__ mask, const int32_t* __restrict__ idx, int ncap,
+    uint16_t* __restrict__ xq16, float* __restrict__ rowabs, uint16_t* __restrict__ xout,
+    uint16_t* __restrict__ wout, int8_t* __restrict__ xq8) {
+  extern __shared__ uint32_t s_mask[];  // (in + 31) / 32 words
+  __shared__ uint32_t s_red[kRowThreads / 32];
+  const int n = hdr->n_out_used;
+  const int npad = (n + 63) / 64 * 64;
+  if (blockIdx.x < (unsigned)T) {
+    const int words = (in + 31) / 32;
+    for (int w = threadIdx.x; w < words; w += kRowThreads) s_mask[w] = __ldg(&mask[w]);
+    __syncthreads();
+    const size_t i = blockIdx.x;
+    const uint16_t* x = X + i * in;
+    const float a = quantize_row<true>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
+                                       xq16 + i * in, s_red);
+    if (threadIdx.x == 0) rowabs[i] = a;
+    for (int k = threadIdx.x; k < npad; k += kRowThreads)
+      xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
+  } else {
+    if (npad == 0) return;
+    const int o = (blockIdx.x - T) * 32 + (threadIdx.x >> 3);
+    if (o >= out) return;
+    const float scb = __ldg(&SCB[o]);
+    for (int k = threadIdx.x & 7; k < npad; k += 8) {
+      uint16_t v = 0;
+      if (k < n) {
+        const float c = (float)__ldg(&CB[(size_t)o * in + __ldg(&idx[k])]);
+        v = __half_as_ushort(__float2half_rn(__fdiv_rn(__fmul_rn(c, scb), 127.0f)));
+      }
+      wout[(size_t)o * ncap + k] = v;
+    }
+  }
+}
+
+// Zeropoint rows: S = 254/(max-min), Z = rint(S*min) + 127, code = clamp(rint(x*S - Z)).
+__global__ void __launch_bounds__(kRowThreads) zeropoint_rows_kernel(
+    const uint16_t* __restrict__ X, int cols, int8_t* __restrict__ Q, float* __restrict__ S,
+    float* __restrict__ Z) {
+  __shared__ float s_mn[kRowThreads / 32], s_mx[kRowThreads / 32];
+  const size_t row = blockIdx.x;
+  const uint16_t* x = X + row * cols;
+  int8_t* q = Q + row * cols;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int j = threadIdx.x; j < cols; j += kRowThreads) {
+    const float v = h2f(x[j]);
+    mn = fminf(mn, v);
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { s_mn[warp] = mn; s_mx[warp] = mx; }
+  __syncthreads();
+  mn = s_mn[0];
+  mx = s_mx[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) { mn = fminf(mn, s_mn[w]); mx = fmaxf(mx, s_mx[w]); }
+  if (cols == 0) { mn = 0.0f; mx = 0.0f; }
+  if (mx > mn) {
+    const float sc = __fdiv_rn(254.0f, __fsub_rn(mx, mn));
+    const float z = __fadd_rn(rintf(__fmul_rn(sc, mn)), 127.0f);
+    if (threadIdx.x == 0) { S[row] = sc; Z[row] = z; }
+    for (int j = threadIdx.x; j < cols; j += kRowThreads) {
+      const int c = __float2int_rn(__fsub_rn(__fmul_rn(h2f(x[j]), sc), z));
+      q[j] = (int8_t)max(-127, min(127, c));
+    }
+  } else {
+    if (threadIdx.x == 0) { S[row] = 0.0f; Z[row] = mn; }
+    for (int j = threadIdx.x; j < cols; j += kRowThreads) q[j] = 0;
+  }
+}
+
+cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
+                               cudaStream_t s) {
+  absmax_rows_kernel<<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), cols, Q,
+                                                   absmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
+                                  float* Z, cudaStream_t s) {
+  zeropoint_rows_kernel<<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), cols, Q,
+                                                      S, Z);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* CB,
+                                   const float* SCB, int out, const WsHeader* hdr,
+                                   const uint32_t* mask, const int32_t* idx, int ncap,
+                                   void* xq16, float* rowabs, void* xout, void* wout,
+                                   int8_t* xq8_debug, cudaStream_t s) {
+  const int wblocks = (out + 31) / 32;
+  const size_t smem = sizeof(uint32_t) * (size_t)((in + 31) / 32);
+  quantize_gather_kernel<<<T + wblocks, kRowThreads, smem, s>>>(
+      static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,
+      static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),
+      static_cast<uint16_t*>(wout), xq8_debug);
+  return cudaGetLastError();
+}
+
+}  // namespace i8mm

@@ -1,0 +1,242 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle.
+
+Bit-exact: outlier column sets, int8 codes, row absmax, CB/SCB, int32 accumulators,
+zeropoint codes/S/Z. Floating point: |y - y_ref| <= 2e-2 + 2e-3 |y_ref| for the fp16 output
+against the oracle's fp64 evaluation of the same quantized definition.
+"""
+import functools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def i8():
+    import int8_mixed_precision_03_b300 as m
+    from int8_mixed_precision_03_b300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@functools.lru_cache(maxsize=2)
+def _weights(d_out, d_in, w_std, seed):
+    w = synth.Workload("w", 1, d_in, d_out, w_std=w_std, seed=seed)
+    W = synth.make_w(w)
+    return W, synth.make_bias(w), oracle.quantize_weight(W)
+
+
+def weights(w):
+    """W, bias and the oracle's CB/SCB, shared by configs with the same weight shape."""
+    return _weights(w.d_out, w.d_in, w.w_std, w.seed)
+
+
+def sample_rows(T, k=8, seed=0):
+    g = np.random.default_rng(seed)
+    base = {0, T - 1, T // 2}
+    extra = g.choice(T, size=min(T, k), replace=False)
+    return np.array(sorted(base | set(int(e) for e in extra)), dtype=np.int64)
+
+
+def check_y(Y, ref):
+    Y = Y.astype(np.float64)
+    err = np.abs(Y - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; worst err "
+                           f"{err.max():.4g} at ref {ref.flat[err.argmax()]:.4g}")
+
+
+def run_and_compare(i8, X, W, bias, threshold, rows=None, CBo=None, SCBo=None,
+                    check_weights=True):
+    if CBo is None:
+        CBo, SCBo = oracle.quantize_weight(W)
+    Wd = dev(W)
+    CB, SCB = i8.int8_quantize_weight(Wd)
+    if check_weights:
+        assert torch.equal(CB.cpu(), torch.from_numpy(CBo)), "CB codes differ"
+        assert torch.equal(SCB.cpu(), torch.from_numpy(SCBo)), "SCB differs"
+    r = i8.int8_matmul_debug(dev(X), CB, SCB, threshold,
+                             None if bias is None else dev(bias))
+    assert i8.i8_get_status(r["workspace"]) == 0
+    T = X.shape[0]
+    rows = np.arange(T) if rows is None else rows
+    ref = oracle.int8_matmul(X, CBo, SCBo, threshold=threshold, bias=bias, rows=rows)
+    assert r["idx"].cpu().numpy().tolist() == ref["idx"].tolist(), "outlier set differs"
+    Xq = r["Xq"].cpu().numpy()[rows]
+    np.testing.assert_array_equal(Xq, ref["Q"])
+    np.testing.assert_array_equal(r["rowabs"].cpu().numpy()[rows], ref["rowabs"])
+    acc = r["acc"].cpu().numpy()[rows].astype(np.int64)
+    np.testing.assert_array_equal(acc, ref["acc"])
+    check_y(r["Y"].cpu().numpy()[rows], ref["Y"])
+    # the plain entry point gives the same output as the debug one
+    Y2 = i8.int8_matmul(dev(X), CB, SCB, threshold, None if bias is None else dev(bias))
+    assert torch.equal(Y2, r["Y"])
+    return r, ref
+
+
+# ----------------------------------------------------------------- small and ragged shapes
+def test_tiny_config(i8):
+    w = synth.WORKLOADS["tiny"]
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    r, ref = run_and_compare(i8, X, W, bias, w.threshold)
+    assert r["n_out"] == 2
+
+
+@pytest.mark.parametrize("T,d,out,k", [
+    (1, 16, 1, 0), (2, 48, 7, 1), (7, 64, 129, 3), (8, 128, 100, 15), (9, 256, 257, 16),
+    (63, 1040, 300, 17), (64, 2064, 128, 65), (65, 512, 384, 0), (129, 1024, 520, 5),
+    (300, 3072, 640, 40), (257, 4096, 255, 2),
+])
+def test_ragged_shapes(i8, T, d, out, k):
+    w = synth.Workload("ragged", T, d, out, n_outlier_cols=k, row_frac=0.7, seed=T * 7 + d)
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    run_and_compare(i8, X, W, bias, 6.0)
+
+
+def test_no_bias_zero_row_and_all_outlier_row(i8):
+    w = synth.Workload("edge", 40, 512, 300, n_outlier_cols=6, row_frac=1.0, seed=3)
+    X, W = synth.make_x(w), synth.make_w(w)
+    X[5] = 0                                            # zero row: absmax 0, codes 0
+    cols = synth.outlier_columns(w)
+    X[9] = 0
+    X[9, cols] = 50                                     # a row made only of outliers
+    W[17] = 0                                           # zero weight row: SCB 0
+    run_and_compare(i8, X, W, None, 6.0)
+
+
+def test_threshold_inf_and_threshold_edge(i8):
+    w = synth.Workload("thr", 33, 256, 200, n_outlier_cols=3, seed=11)
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    X[4, 10] = 6.0                                      # exactly at threshold: outlier
+    X[6, 11] = np.float16(5.99609375)                   # just below: inlier
+    r, _ = run_and_compare(i8, X, W, bias, 6.0)
+    got = r["idx"].cpu().numpy().tolist()
+    assert 10 in got and 11 not in got
+    r, _ = run_and_compare(i8, X, W, bias, math.inf)
+    assert r["n_out"] == 0
+
+
+@pytest.mark.parametrize("pattern", ["same_sign", "alternating", "random"])
+def test_int32_accumulator_exact_at_extreme_codes(i8, pattern):
+    """Codes of +-127 everywhere make every fp32 chunk sum as large as the method allows
+    (1024 * 127^2 < 2^24); the int32 result must still be exact."""
+    T, d, out = 160, 4096, 256
+    g = np.random.default_rng(5)
+    if pattern == "same_sign":
+        sx = np.ones((T, d)); sw = np.ones((out, d))
+        sx[1::2] = -1
+    elif pattern == "alternating":
+        sx = np.where(np.arange(d) % 2 == 0, 1.0, -1.0)[None, :].repeat(T, 0)
+        sw = np.where(np.arange(d) % 3 == 0, 1.0, -1.0)[None, :].repeat(out, 0)
+    else:
+        sx = g.choice([-1.0, 1.0], (T, d)); sw = g.choice([-1.0, 1.0], (out, d))
+    # +-127 * 2^-10: every code is +-127 (the row scale cancels) and Y stays finite in fp16
+    X = (127 * sx / 1024).astype(np.float16)
+    W = (127 * sw / 1024).astype(np.float16)
+    r, ref = run_and_compare(i8, X, W, None, math.inf)
+    exact = (127 * sx).astype(np.int64) @ (127 * sw).astype(np.int64).T
+    np.testing.assert_array_equal(r["acc"].cpu().numpy().astype(np.int64), exact)
+    assert np.abs(exact).max() == 4096 * 127 * 127 or pattern != "same_sign"
+
+
+def test_outlier_capacity_exceeded_sets_status(i8):
+    w = synth.Workload("cap", 16, 1024, 128, n_outlier_cols=100, row_frac=1.0, seed=2)
+    X, W = synth.make_x(w), synth.make_w(w)
+    CB, SCB = i8.int8_quantize_weight(dev(W))
+    ws = i8.alloc_workspace(16, 1024, 128, "cuda", max_outlier_cols=64)
+    i8.int8_matmul(dev(X), CB, SCB, 6.0, workspace=ws)
+    assert i8.i8_get_status(ws) == 6
+    ws = i8.alloc_workspace(16, 1024, 128, "cuda", max_outlier_cols=128)
+    i8.int8_matmul(dev(X), CB, SCB, 6.0, workspace=ws)
+    assert i8.i8_get_status(ws) == 0
+
+
+def test_workspace_reuse_across_calls(i8):
+    """The header is reset per call: a second call on the same workspace is unaffected by
+    the first one's outlier set."""
+    wa = synth.Workload("a", 24, 512, 256, n_outlier_cols=9, seed=21)
+    wb = synth.Workload("b", 24, 512, 256, n_outlier_cols=0, seed=22)
+    ws = i8.alloc_workspace(24, 512, 256, "cuda")
+    for w in (wa, wb, wa):
+        X, W = synth.make_x(w), synth.make_w(w)
+        CBo, SCBo = oracle.quantize_weight(W)
+        CB, SCB = i8.int8_quantize_weight(dev(W))
+        r = i8.int8_matmul_debug(dev(X), CB, SCB, 6.0, workspace=ws)
+        ref = oracle.int8_matmul(X, CBo, SCBo, threshold=6.0)
+        assert r["idx"].cpu().numpy().tolist() == ref["idx"].tolist()
+        check_y(r["Y"].cpu().numpy(), ref["Y"])
+
+
+# ----------------------------------------------------------------- standalone quantizers
+@pytest.mark.parametrize("rows,cols", [(1024, 8192), (3, 7), (5, 1000), (17, 40), (2, 1)])
+def test_absmax_rows_bit_exact(i8, rows, cols):
+    X = synth.make_random_f16(rows * 31 + cols, (rows, cols), std=1.5)
+    X[0, :] = 0
+    Q, a = i8.absmax_quantize_rows(dev(X))
+    Qo, ao = oracle.quantize_rows_absmax(X)
+    np.testing.assert_array_equal(Q.cpu().numpy(), Qo)
+    np.testing.assert_array_equal(a.cpu().numpy(), ao)
+
+
+@pytest.mark.parametrize("rows,cols", [(1024, 8192), (4, 9), (6, 1000), (3, 1)])
+def test_zeropoint_rows_bit_exact(i8, rows, cols):
+    w = synth.Workload("zp", rows, cols, 1)
+    X = synth.make_relu_like(w)
+    if rows > 3:
+        X[3] = 2.5                       # constant row
+        X[2] = -X[2]                     # a non-negative row turned non-positive
+    Q, S, Z = i8.zeropoint_quantize_rows(dev(X))
+    Qo, So, Zo = oracle.zeropoint_rows(X)
+    np.testing.assert_array_equal(Q.cpu().numpy(), Qo)
+    np.testing.assert_array_equal(S.cpu().numpy(), So)
+    np.testing.assert_array_equal(Z.cpu().numpy(), Zo)
+
+
+@pytest.mark.parametrize("out,d", [(1024, 256), (37, 100), (5, 16)])
+def test_weight_quantize_bit_exact(i8, out, d):
+    W = synth.make_random_f16(out + d, (out, d), std=0.02)
+    CB, SCB = i8.int8_quantize_weight(dev(W))
+    CBo, SCBo = oracle.quantize_weight(W)
+    np.testing.assert_array_equal(CB.cpu().numpy(), CBo)
+    np.testing.assert_array_equal(SCB.cpu().numpy(), SCBo)
+
+
+@pytest.mark.parametrize("T,d,out", [(16, 256, 1024), (300, 1040, 520), (2048, 4096, 1024)])
+def test_f16_matmul_comparator(i8, T, d, out):
+    X = synth.make_random_f16(T + d, (T, d))
+    W = synth.make_random_f16(out + d + 1, (out, d), std=0.02)
+    b = synth.make_random_f16(out, (out,), std=0.01)
+    Y = i8.f16_matmul(dev(X), dev(W), dev(b)).cpu().numpy().astype(np.float64)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T + b.astype(np.float64)
+    check_y(Y, ref)
+
+
+# ----------------------------------------------------------------- full-size configurations
+FULL = ["ffn_6.7b_up", "ffn_13b_up", "ffn_13b_down", "decode_176b_t1", "decode_176b_t8",
+        "decode_176b_t64", "sweep_f0_thr6", "sweep_f0.1_thr6", "sweep_f0.5_thr6",
+        "sweep_f2_thr6", "sweep_f2_thrinf"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config_sampled_rows(i8, name):
+    w = synth.WORKLOADS[name]
+    X = synth.make_x(w)
+    W, bias, (CBo, SCBo) = weights(w)
+    rows = sample_rows(w.T)
+    r, ref = run_and_compare(i8, X, W, bias, w.threshold, rows=rows, CBo=CBo, SCBo=SCBo)
+    planted = synth.outlier_columns(w)
+    if w.threshold == 6.0:
+        assert set(planted.tolist()) <= set(ref["idx"].tolist())
