@@ -151,6 +151,15 @@ const char* i8_status_string(i8_status s);
 /* Number of kernels (and memsets) the last successful call on this host thread launched. */
 int i8_last_launch_count(void);
 
+/*
+ * Profiling aid. `events` is NULL (off) or an array of 4 cudaEvent_t handles owned by the
+ * caller. While set, every int8_matmul / int8_matmul_debug on this host thread records
+ * events[0] before the column statistics, events[1] before the quantize pass, events[2]
+ * before the tensor-core matmul and events[3] after it, on the call's stream, so that the
+ * caller can time each kernel with cudaEventElapsedTime. Changes nothing else.
+ */
+void i8_set_profile_events(void** events);
+
 #ifdef __cplusplus
 }
 #endif

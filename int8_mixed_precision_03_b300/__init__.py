@@ -34,6 +34,7 @@ SIGNATURES = {
     "i8_get_status": (_i, [_p, _p]),
     "i8_status_string": (C.c_char_p, [_i]),
     "i8_last_launch_count": (_i, []),
+    "i8_set_profile_events": (None, [_p]),
 }
 
 _lib = None
@@ -194,3 +195,16 @@ def i8_get_status(workspace: torch.Tensor) -> int:
 
 def i8_last_launch_count() -> int:
     return int(lib().i8_last_launch_count())
+
+
+def i8_set_profile_events(events) -> None:
+    """events: None, or 4 torch.cuda.Event(enable_timing=True) recorded around the three
+    kernels of every following int8_matmul on this thread."""
+    if events is None:
+        lib().i8_set_profile_events(None)
+        return
+    for e in events:  # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record()
+    arr = (C.c_void_p * 4)(*[C.c_void_p(e.cuda_event) for e in events])
+    lib().i8_set_profile_events(C.cast(arr, C.c_void_p))

@@ -11,6 +11,11 @@ namespace i8mm {
 namespace {
 
 thread_local int g_last_launches = 0;
+thread_local cudaEvent_t g_prof[4] = {nullptr, nullptr, nullptr, nullptr};
+
+void prof_mark(int i, cudaStream_t s) {
+  if (g_prof[i]) cudaEventRecord(g_prof[i], s);
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -88,15 +93,18 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
 
   if (cudaMemsetAsync(ws, 0, L.zero_bytes, s) != cudaSuccess) return I8_ERR_CUDA;
   ++g_last_launches;
+  prof_mark(0, s);
   if ((st = from_cuda(launch_colstats(X, T, in, threshold_to_half_bits(threshold), hdr, mask,
                                       idx, ncap, s))) != I8_OK)
     return st;
   ++g_last_launches;
+  prof_mark(1, s);
   if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
                                              ws + L.xq, rowabs, ws + L.xout, ws + L.wout,
                                              dbg_xq, s))) != I8_OK)
     return st;
   ++g_last_launches;
+  prof_mark(2, s);
   GemmArgs g;
   g.a_int8 = CB;
   g.b_f16 = ws + L.xq;
@@ -114,6 +122,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   g.out = out;
   if ((st = from_cuda(launch_gemm(g, s))) != I8_OK) return st;
   ++g_last_launches;
+  prof_mark(3, s);
   // debug copies of the intermediates (stream-ordered device copies)
   if (dbg_idx && cudaMemcpyAsync(dbg_idx, idx, sizeof(int32_t) * (size_t)in,
                                  cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -243,3 +252,8 @@ I8_API const char* i8_status_string(i8_status s) {
 }
 
 I8_API int i8_last_launch_count(void) { return g_last_launches; }
+
+I8_API void i8_set_profile_events(void** events) {
+  for (int i = 0; i < 4; ++i)
+    g_prof[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+}
