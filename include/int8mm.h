@@ -52,7 +52,8 @@ typedef enum {
   I8_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103 */
   I8_ERR_CUDA = 5,               /* a CUDA runtime call failed (launch, tensor map, ...) */
   I8_ERR_OUTLIER_CAP = 6,        /* device: more outlier columns than the workspace holds */
-  I8_ERR_TIMEOUT = 7             /* device: a pipeline wait gave up (kernel unwound safely) */
+  I8_ERR_TIMEOUT = 7,            /* device: a pipeline wait gave up (kernel unwound safely) */
+  I8_ERR_SCRATCH_LIMIT = 8       /* int8_matmul_noalloc: sizes exceed its built-in scratch */
 } i8_status;
 
 /* Largest supported `in`: keeps |acc| <= 127*127*in below 2^31. */
@@ -150,6 +151,36 @@ const char* i8_status_string(i8_status s);
 
 /* Number of kernels (and memsets) the last successful call on this host thread launched. */
 int i8_last_launch_count(void);
+
+/* Size of the built-in device scratch used by int8_matmul_noalloc (32 MiB per GPU). */
+#define I8_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * int8_matmul without a caller-provided workspace, for callers that cannot allocate device
+ * memory when they call: applications whose device memory is handed out only by their own
+ * allocator (plug-ins, embedded inference runtimes), latency-critical loops that must not
+ * call cudaMalloc (it can synchronize the device and takes a driver-wide lock), and code
+ * that runs where allocation is not allowed at all. The pages have no counterpart to this
+ * call; it is a deployment convenience.
+ *
+ * Arguments, layouts, results and errors are those of int8_matmul minus the workspace.
+ * The scratch is a fixed array of I8_NOALLOC_SCRATCH_BYTES in device memory that every GPU
+ * which loads this library reserves until the process exits. Sizes whose workspace (with a
+ * 64-column outlier capacity) does not fit return I8_ERR_SCRATCH_LIMIT before any launch;
+ * within the limit the outlier capacity is the largest multiple of 64 columns that fits.
+ * Roughly: 2*T*in + 128*(T + out) + 4*in bytes plus a few KB must fit in 32 MiB.
+ * - The first call on a device looks up the scratch's device address (once per device,
+ *   with that device current); make that first call before any stream capture.
+ * - All calls share the one scratch and it keeps the last call's contents; the parts that
+ *   must start at zero are cleared by every call. Calls that overlap on the GPU (other
+ *   streams, other host threads) race on the scratch: serialize them.
+ * - The device status word lives in the scratch and is not readable through
+ *   i8_get_status; more outlier columns than the capacity makes Y wrong silently.
+ * Calls no allocating routine.
+ */
+i8_status int8_matmul_noalloc(const void* X, int T, int in, const int8_t* CB, const float* SCB,
+                              int out, float threshold, const void* bias, void* Y,
+                              void* stream);
 
 /*
  * Profiling aid. `events` is NULL (off) or an array of 4 cudaEvent_t handles owned by the

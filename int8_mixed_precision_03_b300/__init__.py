@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libint8mm.so")
 I8_OK = 0
 STATUS = {0: "I8_OK", 1: "I8_ERR_INVALID_ARG", 2: "I8_ERR_ALIGNMENT", 3: "I8_ERR_WORKSPACE",
           4: "I8_ERR_UNSUPPORTED_DEVICE", 5: "I8_ERR_CUDA", 6: "I8_ERR_OUTLIER_CAP",
-          7: "I8_ERR_TIMEOUT"}
+          7: "I8_ERR_TIMEOUT", 8: "I8_ERR_SCRATCH_LIMIT"}
 
 # Every symbol the header declares, with its ctypes signature.
 _p, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
@@ -26,6 +26,7 @@ SIGNATURES = {
     "int8_quantize_weight": (_i, [_p, _i, _i, _p, _p, _p]),
     "int8_matmul_workspace_size": (_sz, [_i, _i, _i, _i]),
     "int8_matmul": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p, _sz, _p]),
+    "int8_matmul_noalloc": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p]),
     "int8_matmul_debug": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p, _sz, _p,
                                _p, _p, _p, _p, _p]),
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
@@ -124,6 +125,24 @@ def int8_matmul(X: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, threshold:
     _check("int8_matmul", lib().int8_matmul(
         _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
         _ptr(workspace), workspace.numel(), _stream(X.device)))
+    return Y
+
+
+def int8_matmul_noalloc(X: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor,
+                        threshold: float = 6.0, bias: torch.Tensor | None = None,
+                        Y: torch.Tensor | None = None) -> torch.Tensor:
+    """int8_matmul on the library's built-in device scratch instead of a workspace, for
+    callers that cannot allocate device memory at call time (pass a preallocated Y)."""
+    _need(X, torch.float16, "X")
+    _need(CB, torch.int8, "CB")
+    _need(SCB, torch.float32, "SCB")
+    T, d = X.shape
+    out = CB.shape[0]
+    if Y is None:
+        Y = torch.empty((T, out), dtype=torch.float16, device=X.device)
+    _check("int8_matmul_noalloc", lib().int8_matmul_noalloc(
+        _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
+        _stream(X.device)))
     return Y
 
 

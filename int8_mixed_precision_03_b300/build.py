@@ -12,7 +12,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libint8mm.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["capi.cu", "colstats.cu", "quantize.cu", "gemm.cu"]
+SOURCES = ["capi.cu", "colstats.cu", "quantize.cu", "gemm.cu", "noalloc.cu"]
 HEADERS = ["int8mm_internal.h", "sm103_ptx.cuh", os.path.join("..", "..", "include", "int8mm.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -247,6 +247,7 @@ I8_API const char* i8_status_string(i8_status s) {
     case I8_ERR_CUDA: return "CUDA runtime error";
     case I8_ERR_OUTLIER_CAP: return "more outlier columns than the workspace capacity";
     case I8_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case I8_ERR_SCRATCH_LIMIT: return "sizes exceed the built-in scratch of int8_matmul_noalloc";
   }
   return "unknown status";
 }
