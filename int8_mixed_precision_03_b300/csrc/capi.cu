@@ -90,6 +90,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   uint32_t* mask = reinterpret_cast<uint32_t*>(ws + L.mask);
   int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
   float* rowabs = reinterpret_cast<float*>(ws + L.rowabs);
+  int32_t* l1 = reinterpret_cast<int32_t*>(ws + L.l1);
 
   if (cudaMemsetAsync(ws, 0, L.zero_bytes, s) != cudaSuccess) return I8_ERR_CUDA;
   ++g_last_launches;
@@ -101,7 +102,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   prof_mark(1, s);
   if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
                                              ws + L.xq, rowabs, ws + L.xout, ws + L.wout,
-                                             dbg_xq, s))) != I8_OK)
+                                             l1, dbg_xq, s))) != I8_OK)
     return st;
   ++g_last_launches;
   prof_mark(2, s);
@@ -113,6 +114,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   g.ncap = ncap;
   g.hdr = hdr;
   g.rowabs = rowabs;
+  g.l1 = l1;
   g.scb = SCB;
   g.bias = bias;
   g.Y = Y;

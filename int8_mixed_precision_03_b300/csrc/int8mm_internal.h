@@ -11,6 +11,15 @@ namespace i8mm {
 constexpr int kSmCount = 148;       // B300: 2 dies x 74 SMs
 constexpr int kKBlock = 64;         // K elements per pipeline stage (128 bytes of fp16)
 constexpr int kChunkKBlocks = 16;   // K blocks per exact fp32 accumulation chunk (1024 K)
+constexpr int kChunkK = kKBlock * kChunkKBlocks;
+
+// Token tile (MMA N) of the tensor-core matmul for T tokens: the smallest supported size
+// that covers T, 256 for large T. The quantize pass uses it to group its per-chunk code
+// statistics by token tile.
+inline int gemm_bn(int T) {
+  return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256;
+}
+inline int num_chunks(int in) { return (in + kChunkK - 1) / kChunkK; }
 
 // Device status header at the start of every int8_matmul workspace (zeroed per call).
 struct WsHeader {
@@ -25,8 +34,9 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 // Byte offsets of the int8_matmul workspace sections. Computed identically by
 // int8_matmul_workspace_size() and int8_matmul().
 struct WsLayout {
-  size_t header = 0, mask = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0, total = 0;
-  size_t zero_bytes = 0;  // header + mask: memset at the start of every call
+  size_t header = 0, mask = 0, l1 = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0;
+  size_t total = 0;
+  size_t zero_bytes = 0;  // header + mask + l1: memset at the start of every call
   int words = 0;          // 32-column words of the outlier mask
   int ncap = 0;           // outlier column capacity (multiple of 64)
 };
@@ -40,6 +50,10 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.ncap = ncap;
   L.header = off; off += sizeof(WsHeader);
   L.mask = off; off = align_up(off + sizeof(uint32_t) * L.words, 256);
+  // per (token tile, 1024-K chunk): max over the tile's rows of sum |code| in the chunk
+  L.l1 = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)((T + gemm_bn(T) - 1) / gemm_bn(T)) *
+                           num_chunks(in), 256);
   L.zero_bytes = off;
   L.idx = off; off = align_up(off + sizeof(int32_t) * (size_t)in, 256);
   L.xq = off; off = align_up(off + 2 * (size_t)T * in, 256);
@@ -60,7 +74,7 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
                                    const float* SCB, int out, const WsHeader* hdr,
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
-                                   int8_t* xq8_debug, cudaStream_t s);
+                                   int32_t* l1, int8_t* xq8_debug, cudaStream_t s);
 cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
                                cudaStream_t s);
 cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
@@ -79,6 +93,7 @@ struct GemmArgs {
   int ncap = 0;
   WsHeader* hdr = nullptr;      // status word + n_out (int8 path), may be null for fp16
   const float* rowabs = nullptr;
+  const int32_t* l1 = nullptr;  // per (token tile, chunk) code-magnitude bounds, or null
   const float* scb = nullptr;
   const void* bias = nullptr;
   void* Y = nullptr;

@@ -49,11 +49,13 @@ __device__ __forceinline__ bool is_masked(const uint32_t* smask, int j) {
 // Quantizes one row of `cols` fp16 values.
 //   kMasked: columns flagged in smask are excluded from the absmax and coded 0.
 //   q8 (nullable): int8 codes; q16 (nullable): the same codes as exact fp16 values.
+//   s_l1 (nullable, shared, zeroed): += sum of |code| per 1024-column chunk.
 // Returns the row absmax (over unmasked columns).
 template <bool kMasked>
 __device__ float quantize_row(const uint16_t* __restrict__ x, int cols,
                               const uint32_t* smask, int8_t* __restrict__ q8,
-                              uint16_t* __restrict__ q16, uint32_t* s_red) {
+                              uint16_t* __restrict__ q16, uint32_t* s_red,
+                              int* s_l1 = nullptr) {
   const int tid = threadIdx.x;
   const bool vec = (cols & 7) == 0;
   uint32_t mx = 0;  // running max of |x| bit patterns
@@ -100,6 +102,12 @@ __device__ float quantize_row(const uint16_t* __restrict__ x, int cols,
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           if ((mb >> e) & 1u) q[e] = 0;
+      }
+      if (s_l1) {
+        int a1 = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a1 += abs(q[e]);
+        atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
       }
       if (q8) {
         uint2 o;
@@ -149,20 +157,27 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
     const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
     const uint32_t* __restrict__ mask, const int32_t* __restrict__ idx, int ncap,
     uint16_t* __restrict__ xq16, float* __restrict__ rowabs, uint16_t* __restrict__ xout,
-    uint16_t* __restrict__ wout, int8_t* __restrict__ xq8) {
+    uint16_t* __restrict__ wout, int32_t* __restrict__ l1, int bn, int8_t* __restrict__ xq8) {
   extern __shared__ uint32_t s_mask[];  // (in + 31) / 32 words
   __shared__ uint32_t s_red[kRowThreads / 32];
+  __shared__ int s_l1[I8_MAX_IN / kChunkK];
   const int n = hdr->n_out_used;
   const int npad = (n + 63) / 64 * 64;
   if (blockIdx.x < (unsigned)T) {
     const int words = (in + 31) / 32;
+    const int nch = (in + kChunkK - 1) / kChunkK;
     for (int w = threadIdx.x; w < words; w += kRowThreads) s_mask[w] = __ldg(&mask[w]);
+    for (int c = threadIdx.x; c < nch; c += kRowThreads) s_l1[c] = 0;
     __syncthreads();
     const size_t i = blockIdx.x;
     const uint16_t* x = X + i * in;
     const float a = quantize_row<true>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
-                                       xq16 + i * in, s_red);
+                                       xq16 + i * in, s_red, s_l1);
     if (threadIdx.x == 0) rowabs[i] = a;
+    __syncthreads();
+    // bound of the matmul's fp32 chunk sums: max over the token tile of sum |code|
+    for (int c = threadIdx.x; c < nch; c += kRowThreads)
+      if (s_l1[c] > 0) atomicMax(&l1[(size_t)(i / bn) * nch + c], s_l1[c]);
     for (int k = threadIdx.x; k < npad; k += kRowThreads)
       xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
   } else {
@@ -240,13 +255,13 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
                                    const float* SCB, int out, const WsHeader* hdr,
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
-                                   int8_t* xq8_debug, cudaStream_t s) {
+                                   int32_t* l1, int8_t* xq8_debug, cudaStream_t s) {
   const int wblocks = (out + 31) / 32;
   const size_t smem = sizeof(uint32_t) * (size_t)((in + 31) / 32);
   quantize_gather_kernel<<<T + wblocks, kRowThreads, smem, s>>>(
       static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,
       static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),
-      static_cast<uint16_t*>(wout), xq8_debug);
+      static_cast<uint16_t*>(wout), l1, gemm_bn(T), xq8_debug);
   return cudaGetLastError();
 }
 
