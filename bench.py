@@ -35,6 +35,9 @@ import synth  # noqa: E402
 METRIC = "int8_matmul TOPS and % of INT8-tensor/HBM roofline on T×d→4d FFN GEMM"
 UNIT = "TOPS"
 DEFAULT_WORKLOAD = "ffn_6.7b_up"
+ALL_CONFIGS = ["ffn_6.7b_up", "ffn_13b_up", "ffn_13b_down", "decode_176b_t1", "decode_176b_t8",
+               "decode_176b_t64", "sweep_f0_thr6", "sweep_f0.1_thr6", "sweep_f0.5_thr6",
+               "sweep_f2_thr6", "sweep_f0_thrinf", "sweep_f2_thrinf"]
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -82,6 +85,39 @@ def algorithmic_bytes(w: synth.Workload) -> int:
     return 2 * w.T * w.d_in + w.d_in * w.d_out + 4 * w.d_out + 2 * w.d_out + 2 * w.T * w.d_out
 
 
+def gemm_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of the matmul kernel: CB, the fp16 activation codes, SCB, rowabs,
+    bias and Y (the outlier slices are a few KB and are left out)."""
+    return w.d_in * w.d_out + 2 * w.T * w.d_in + 4 * w.d_out + 4 * w.T + 2 * w.d_out \
+        + 2 * w.T * w.d_out
+
+
+def hbm_bound(w: synth.Workload) -> bool:
+    """Decode shapes (T <= 64): streaming CB from HBM takes longer than the tensor work."""
+    return w.T <= 64
+
+
+def roofline(w: synth.Workload, gemm_ms: float, peaks: dict, peak_src: str) -> dict:
+    """Roofline of the dominant kernel (the tensor-core matmul), from its CUDA-event time."""
+    s = gemm_ms / 1e3
+    traffic = measured_traffic(w.name)
+    if hbm_bound(w):
+        achieved = gemm_bytes(w) / s / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes": gemm_bytes(w),
+                "kernel": "gemm (tcgen05 kind::f16 on exact int8 codes), decode tile",
+                "peak_source": f"hbm_gbs, {peak_src} (MEASURED_PEAKS.json)"}
+    achieved = workload_ops(w) / s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "kernel": "gemm (tcgen05 kind::f16 on exact int8 codes)",
+            "peak_source": f"bf16_tflops burst, {peak_src} (MEASURED_PEAKS.json); the int8 "
+                           "product runs on kind::f16, at the bf16/fp16 rate"}
+
+
 # ------------------------------------------------------------------ distributed plumbing
 def dist_env() -> tuple[int, int, int]:
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -109,70 +145,99 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons; only the samples taken inside
+    the timed region (between mark_start() and mark_end(), host wall clock) are kept."""
 
     def __init__(self, gpu_index: int):
         self.proc = None
+        self.t0 = self.t1 = None
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
-                 "-i", str(gpu_index), "-lms", "100"],
+                ["nvidia-smi", f"--query-gpu=timestamp,{CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-i", str(gpu_index), "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)   # let the sampler start before the timed region opens
         except OSError:
             self.proc = None
+
+    def mark_start(self) -> None:
+        self.t0 = time.time()
+
+    def mark_end(self) -> None:
+        self.t1 = time.time()
 
     def stop(self) -> dict | None:
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
+        import datetime
+        sm, mx, reasons, total = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
+            total += 1
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm_v, mx_v = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                continue
+            sm.append(sm_v)
+            mx.append(mx_v)
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": f"no sample fell inside the timed region ({total} taken)"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
 def calibrated_rows(w, X, CBo, SCBo, bias, nthreads: int, seconds: float) -> int:
-    """Rows of X whose oracle evaluation takes about `seconds` on these host cores."""
+    """Rows of X whose oracle evaluation takes about `seconds` on these host cores: the
+    per-row cost is the slope between two timed samples (the fixed cost of a call, the
+    outlier scan over all of X, cancels)."""
     import oracle
-    rows = np.linspace(0, w.T - 1, 32).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.int8_matmul(X, CBo, SCBo, w.threshold, bias, rows=rows, nthreads=nthreads,
-                       want_acc=False)
-    dt = max(time.perf_counter() - t0, 1e-3)
-    return int(min(w.T, max(1, round(32 * seconds / dt))))
+
+    def timed(n):
+        rows = np.linspace(0, w.T - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.int8_matmul(X, CBo, SCBo, w.threshold, bias, rows=rows, nthreads=nthreads,
+                           want_acc=False)
+        return time.perf_counter() - t0
+
+    n1, n2 = min(w.T, 4 * nthreads), min(w.T, 16 * nthreads)
+    t1, t2 = timed(n1), timed(n2)
+    per_row = max((t2 - t1) / max(n2 - n1, 1), t2 / n2 * 0.25, 1e-7)
+    fixed = max(t2 - per_row * n2, 0.0)
+    return int(min(w.T, max(1, round((seconds - fixed) / per_row))))
 
 
-def cpu_baseline_sample(w, X, CBo, SCBo, bias, nthreads: int, seconds: float = 10.0) -> dict:
+def cpu_baseline_sample(w, X, CBo, SCBo, bias, nthreads: int, seconds: float = 15.0) -> dict:
     """The oracle as it stands, timed on a bounded sample of rows of the workload."""
     import oracle
     rows_n = calibrated_rows(w, X, CBo, SCBo, bias, nthreads, seconds)
     rows = np.linspace(0, w.T - 1, rows_n).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.int8_matmul(X, CBo, SCBo, threshold=w.threshold, bias=bias, rows=rows,
-                       nthreads=nthreads, want_acc=False)
-    dt = time.perf_counter() - t0
-    ops = 2.0 * rows_n * w.d_in * w.d_out
+    reps, t0 = 0, time.perf_counter()
+    while True:   # the whole workload may take less than `seconds`: repeat it
+        oracle.int8_matmul(X, CBo, SCBo, threshold=w.threshold, bias=bias, rows=rows,
+                           nthreads=nthreads, want_acc=False)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.6 * seconds:
+            break
+    ops = 2.0 * rows_n * w.d_in * w.d_out * reps
     return {"value": ops / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-            "sample": f"{rows_n} of {w.T} rows of {w.name} (outlier scan of all of X, then "
-                      f"quantize, int8 product, fp16 outlier product and bias for those rows), "
-                      f"{dt:.1f} s wall"}
+            "sample": f"{reps} x {rows_n} of {w.T} rows of {w.name} (each pass: outlier scan "
+                      f"of all of X, then quantize, int8 product, fp16 outlier product and "
+                      f"bias for those rows), {dt:.1f} s wall"}
 
 
 def run_reference(args) -> None:
@@ -233,7 +298,6 @@ def run_ours(args) -> None:
     bias = torch.from_numpy(bh).to(device)
     Wd = torch.from_numpy(Wh).to(device)
     CB, SCB = i8.int8_quantize_weight(Wd)        # once per weight, off the timed path
-    del Wd
     ws = i8.alloc_workspace(w.T, w.d_in, w.d_out, device)
     Y = torch.empty((w.T, w.d_out), dtype=torch.float16, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -257,6 +321,8 @@ def run_ours(args) -> None:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
     launches = 0
     for k in range(K):
         flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
@@ -266,6 +332,8 @@ def run_ours(args) -> None:
         ends[k].record()
     i8.i8_set_profile_events(None)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -301,13 +369,26 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     e2e_s, e2e_ops = aggregate(e0.elapsed_time(e1) / 1e3, ops * Ke)
 
+    # our fp16 GEMM on the same shape (the 16-bit comparator), L2 flushed between launches
+    f16_ms = []
+    for k in range(Ke + 3):
+        flush.fill_(k & 0xff)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        i8.f16_matmul(X, Wd, bias, Y=Y)
+        b.record()
+        if k >= 3:
+            f16_ms.append((a, b))
+    torch.cuda.synchronize()
+    f16_ms = statistics.mean(a.elapsed_time(b) for a, b in f16_ms)
+    del Wd
+
     if rank != 0:
         dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
     gemm_ms = statistics.mean(k_ms["gemm"])
-    achieved = ops / (gemm_ms / 1e3) / 1e12
-    peak = float(peaks["bf16_tflops"])
+    roof = roofline(w, gemm_ms, peaks, peak_src)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_s / K * 1e3, "higher_is_better": True,
@@ -317,14 +398,15 @@ def run_ours(args) -> None:
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write, untimed)"},
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": measured_traffic(w.name),
-                     "kernel": "gemm (tcgen05 kind::f16 on exact int8 codes)",
-                     "peak_source": f"bf16_tflops burst, {peak_src} (MEASURED_PEAKS.json); "
-                                    "kind::f16 runs at the bf16 rate"},
+        "roofline": roof,
         "e2e": {"value": e2e_ops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(Xpin.numel() * 2),
                 "d2h_bytes_per_step": int(Ypin.numel() * 2)},
+        "f16_comparator": {"us": round(f16_ms * 1e3, 2),
+                           "TFLOP/s": ops / (f16_ms / 1e3) / 1e12,
+                           "frac_of_bf16_peak": ops / (f16_ms / 1e3) / 1e12
+                           / float(peaks["bf16_tflops"]),
+                           "int8_step_speedup": f16_ms / (total_s / K * 1e3)},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -340,16 +422,25 @@ def run_ours(args) -> None:
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="wall-clock budget of the reference arm's warm-up + timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all", action="store_true",
+                    help="one line per configuration (1 GPU, no CPU baseline)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.all:
+        if dist_env()[1] > 1:
+            raise SystemExit("--all runs on one GPU")
+        args.no_cpu_baseline = True
+        for name in ALL_CONFIGS:
+            args.workload = name
+            run_ours(args)
     else:
         run_ours(args)
 
