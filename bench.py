@@ -52,7 +52,7 @@ def load_peaks() -> tuple[dict, str]:
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 GEMM_SOURCES = [os.path.join(ROOT, "int8_mixed_precision_03_b300", "csrc", f)
-                for f in ("gemm.cu", "sm103_ptx.cuh", "int8mm_internal.h")]
+                for f in ("gemm_i8.cu", "gemm_common.cuh", "sm103_ptx.cuh", "int8mm_internal.h")]
 
 
 def gemm_source_hash() -> str:

@@ -115,6 +115,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   g.hdr = hdr;
   g.rowabs = rowabs;
   g.l1 = l1;
+  g.acc_scratch = reinterpret_cast<int32_t*>(ws + L.acc);
   g.scb = SCB;
   g.bias = bias;
   g.Y = Y;
@@ -122,7 +123,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   g.T = T;
   g.in = in;
   g.out = out;
-  if ((st = from_cuda(launch_gemm(g, s))) != I8_OK) return st;
+  if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
   ++g_last_launches;
   prof_mark(3, s);
   // debug copies of the intermediates (stream-ordered device copies)
@@ -224,7 +225,7 @@ I8_API i8_status f16_matmul(const void* X, int T, int in, const void* W, int out
   g.T = T;
   g.in = in;
   g.out = out;
-  st = from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+  st = from_cuda(launch_f16_gemm(g, static_cast<cudaStream_t>(stream)));
   if (st == I8_OK) g_last_launches = 1;
   return st;
 }

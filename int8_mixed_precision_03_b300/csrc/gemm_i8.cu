@@ -1,0 +1,550 @@
+// Tensor-core matmul of the LLM.int8() method (steps 2 and 3) on tcgen05.
+//
+// "Hugging Face, LLM.int8() ... Transformers and Accelerate" (agentlenshq), section "core
+// idea": the int8 part is multiplied with int8 vector-wise scales, the outlier part in
+// fp16, and the int8 result is dequantized and added to the fp16 result.
+// "LLM.int8() summary" (zenn), section "method": outlier input dimensions and the matching
+// weight dimensions are split off and kept in 16 bit.
+//
+// Exact int8 products on the fp16 tensor path. sm_103a has no int8 tcgen05 MMA (ptxas
+// rejects .kind::i8 for this target), so the int8 product runs on .kind::f16: int8 codes
+// are exact fp16 values and fp32 sums of integers are exact while every partial sum stays
+// within 2^24 in magnitude. The K loop is cut into 1024-element chunks; for each (token
+// tile, chunk) the quantize pass records L1 = max over the tile's rows of sum |code|, and
+// since |CB| <= 127 every partial sum of a run of chunks is bounded by 127 * (sum of their
+// L1). Consecutive chunks share one fp32 accumulation ("segment") while that bound stays
+// <= 2^24; a single chunk always fits (127 * 127 * 1024 < 2^24). At a segment boundary the
+// epilogue converts the fp32 tile to int32 and adds it to a running int32 sum.
+//
+// Tile: M = 128 output features (TMEM lanes) x N = BN tokens (TMEM columns), K stage 64.
+//   A = CB int8 [out, in]: streamed by TMA (64-byte swizzle) into a deep int8 ring; two
+//       sets of four converter warps (alternate K blocks) turn each 128 x 64 block into
+//       fp16 in the 128-byte-swizzled K-major layout in shared memory. The outlier weight
+//       slice W_out fp16 [out, ncap] takes the same route as two 64-byte-wide boxes per K
+//       block, copied without conversion.
+//   B = activation codes as fp16 [T, in] (written by the quantize pass), or the outlier
+//       slice X_out fp16 [T, ncap]: TMA, 128-byte swizzle, K-major.
+//   A and B stages form one ring, released by one MMA commit per K block.
+// TMEM: two accumulators F0 [0, BN) and F1 [BN, 2BN) take the segments in turn (the int
+// segments of a tile, then its outlier segment, then the next tile's), so the epilogue of
+// one segment overlaps the MMAs of the next. The epilogue's running int32 sum of a tile
+// lives in a per-CTA slot of the workspace (L2 resident): a segment that is not the last
+// of its tile is folded into it, and the tile's last segment reads it back.
+// Epilogue: Y[t, o] = fp16(acc * rowabs[t] * SCB[o] / 127^2 + outlier + bias[o]), staged
+// per warp in shared memory (two boxes of tokens x 32 features) and written by TMA stores.
+//
+// Warp roles (512 threads): warp 0 TMA for B, warp 1 MMA issuer and TMEM owner, warp 2 TMA
+// for the weight stream, warps 4-7 and 12-15 converters, warps 8-11 epilogue (warp w
+// reaches TMEM lanes 32*(w%4) .. +31). Persistent CTAs, one per SM, walk tiles
+// token-block fastest so that concurrently running CTAs share the same weight strip in L2.
+#include "gemm_common.cuh"
+
+namespace i8mm {
+namespace gemm {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarpB = 0, kWarpMma = 1, kWarpA8 = 2;
+constexpr int kWarpConv0 = 4, kWarpEpi0 = 8, kWarpConv1 = 12;
+constexpr uint32_t kExactLimit = 1u << 24;                    // integers exact in fp32
+constexpr uint32_t kWorstChunkBound = 127u * 127u * kChunkK;  // < kExactLimit
+static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact");
+
+template <int BN>
+struct Cfg {
+  static constexpr int kW = BN < 32 ? BN : 32;  // tokens per epilogue slice
+  // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring
+  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kStages8 = BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBoxBytes = kW * 32 * 2;
+  static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN;  // F0 + F1
+  // shared memory (stage bases 1024-byte aligned for the swizzled layouts)
+  static constexpr int a16 = 0;
+  static constexpr int b = a16 + kStages * kA16Bytes;
+  static constexpr int a8 = b + kStages * kBBytes;
+  static constexpr int box = a8 + kStages8 * kA8Bytes;
+  static constexpr int bars = box + 4 * 2 * kBoxBytes;
+  // full_a, full_b, empty [kStages]; a8_full, a8_empty [kStages8]; tmem_full,
+  // tmem_empty [2]; done
+  static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * 2 + 1;
+  static constexpr int misc = bars + kNumBars * 8;
+  static constexpr int total = misc + 16 + 1024;  // + alignment slack
+  static_assert(b % 1024 == 0 && kBBytes % 1024 == 0 && a8 % 1024 == 0, "alignment");
+  static_assert(total <= kMaxSmem, "shared memory per CTA");
+};
+
+struct Params {
+  int T, in, out;
+  int m_tiles, n_tiles, nkb;  // nkb = ceil(in / 64)
+  int nchunks;                // ceil(in / 1024)
+  int y_tma;                  // 1: Y written by TMA stores (out % 8 == 0)
+  WsHeader* hdr;
+  const float* rowabs;
+  const int32_t* l1;
+  int32_t* acc_scratch;       // [gridDim.x][BN][128] int32
+  const float* scb;
+  const uint16_t* bias;
+  uint16_t* Y;
+  int32_t* acc_debug;
+  uint64_t timeout_ns;
+  int debug_skip_loads;
+};
+
+__device__ __forceinline__ int outlier_kblocks(const Params& p) {
+  const int n = *reinterpret_cast<volatile const int*>(&p.hdr->n_out_used);
+  return (n + 63) / 64;
+}
+
+// Bound on |partial sums| of chunk c for token tile n_blk (see the file comment).
+__device__ __forceinline__ uint32_t chunk_bound(const Params& p, int n_blk, int c) {
+  if (!p.l1) return kWorstChunkBound;
+  return 127u * (uint32_t)__ldg(&p.l1[(size_t)n_blk * p.nchunks + c]);
+}
+// Greedy rule shared by the MMA issuer and the epilogue: chunk c opens a new segment when
+// it is the first chunk or adding its bound would exceed 2^24.
+struct SegWalker {
+  uint32_t run = 0;
+  __device__ __forceinline__ bool opens(uint32_t b, int c) {
+    if (c == 0 || run + b > kExactLimit) { run = b; return true; }
+    run += b;
+    return false;
+  }
+};
+__device__ __forceinline__ int count_int_segments(const Params& p, int n_blk) {
+  SegWalker w;
+  int n = 0;
+  for (int c = 0; c < p.nchunks; ++c) n += w.opens(chunk_bound(p, n_blk, c), c) ? 1 : 0;
+  return n;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <int BN, bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1)
+    i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmWo, const __grid_constant__ CUtensorMap tmXo,
+                   const __grid_constant__ CUtensorMap tmY, const Params p) {
+  using C = Cfg<BN>;
+  constexpr int kS = C::kStages, kS8 = C::kStages8, kW = C::kW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + C::bars);
+  uint64_t* full_b = full_a + kS;
+  uint64_t* empty = full_b + kS;
+  uint64_t* a8_full = empty + kS;
+  uint64_t* a8_empty = a8_full + kS8;
+  uint64_t* tmem_full = a8_empty + kS8;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* done = tmem_empty + 2;
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::misc);
+  const Abort ab{reinterpret_cast<volatile int*>(smem + C::misc + 4), p.hdr, p.timeout_ns};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&full_a[s], 4);      // the four warps of the converter set
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kS8; ++s) {
+      mbar_init(&a8_full[s], 1);
+      mbar_init(&a8_empty[s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tmem_full[s], 1);
+      mbar_init(&tmem_empty[s], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(done, 1);
+    *ab.flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpB && lane == 0) {
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmXo);
+    tma_prefetch_desc(&tmY);
+  }
+  if (warp == kWarpA8 && lane == 0) {
+    tma_prefetch_desc(&tmA8);
+    tma_prefetch_desc(&tmWo);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(tmem_base_smem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_smem;
+
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int nkb_out = outlier_kblocks(p);
+  const int nkb_all = p.nkb + nkb_out;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == kWarpB) {
+    // -------------------------------------------------------- TMA: B operand
+    if (lane == 0 && !p.debug_skip_loads) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n0 = (t % p.n_tiles) * BN;
+        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+          const uint32_t s = it % kS, ph = (it / kS) & 1u;
+          if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
+          mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
+          if (kb < p.nkb)
+            tma_load_2d(smem + C::b + s * C::kBBytes, &tmB, &full_b[s], kb * BK, n0);
+          else
+            tma_load_2d(smem + C::b + s * C::kBBytes, &tmXo, &full_b[s], (kb - p.nkb) * BK, n0);
+        }
+      }
+      // Do not leave the CTA with copies in flight: wait for the last issued stages.
+      for (uint32_t k = 0; k < (uint32_t)kS && k < it; ++k) {
+        const uint32_t j = it - 1 - k;
+        mbar_wait_bounded(&full_b[j % kS], (j / kS) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == kWarpA8) {
+    // -------------------------------------------------------- TMA: weight stream
+    // One 128 x 64 int8 box per int K block; two 128 x 32 fp16 boxes per outlier K block.
+    if (lane == 0 && !p.debug_skip_loads) {
+      uint32_t i8 = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t / p.n_tiles) * BM;
+        for (int kb = 0; kb < nkb_all && ok; ++kb) {
+          const int nbox = kb < p.nkb ? 1 : 2;
+          for (int h = 0; h < nbox && ok; ++h, ++i8) {
+            const uint32_t s8 = i8 % kS8, ph8 = (i8 / kS8) & 1u;
+            if (!(ok = pipe_wait(&a8_empty[s8], ph8 ^ 1u, ab))) break;
+            mbar_arrive_expect_tx(&a8_full[s8], kA8Bytes);
+            uint8_t* dst = smem + C::a8 + s8 * kA8Bytes;
+            if (kb < p.nkb)
+              tma_load_2d(dst, &tmA8, &a8_full[s8], kb * BK, m0);
+            else
+              tma_load_2d(dst, &tmWo, &a8_full[s8], (kb - p.nkb) * BK + 32 * h, m0);
+          }
+        }
+      }
+      for (uint32_t k = 0; k < (uint32_t)kS8 && k < i8; ++k) {
+        const uint32_t j = i8 - 1 - k;
+        mbar_wait_bounded(&a8_full[j % kS8], (j / kS8) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32acc(BM, BN);
+      uint32_t it = 0, nseg = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n_blk = t % p.n_tiles;
+        SegWalker walker;
+        bool seg_first = true;
+        uint32_t dcol = 0;
+        int c = -1;  // current int chunk
+        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+          // segment boundaries: int chunks grouped by the exactness bound, then the
+          // outlier segment; each segment takes the next accumulator (F0/F1)
+          bool opens = false;
+          if (kb < p.nkb) {
+            if (kb % kChunkKBlocks == 0) {
+              ++c;
+              opens = walker.opens(chunk_bound(p, n_blk, c), c);
+            }
+          } else {
+            opens = kb == p.nkb;
+          }
+          if (opens) {
+            if (kb > 0) { mma_commit(&tmem_full[nseg & 1u]); ++nseg; }
+            if (!(ok = pipe_wait(&tmem_empty[nseg & 1u], ((nseg >> 1) & 1u) ^ 1u, ab))) break;
+            tc_fence_after();
+            dcol = (nseg & 1u) * BN;
+            seg_first = true;
+          }
+          const uint32_t s = it % kS, ph = (it / kS) & 1u;
+          if (!(ok = pipe_wait(&full_a[s], ph, ab))) break;
+          if (!(ok = pipe_wait(&full_b[s], ph, ab))) break;
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
+          const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
+                       (seg_first && k == 0) ? 0u : 1u);
+          seg_first = false;
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tmem_full[nseg & 1u]);
+        ++nseg;
+      }
+      // all issued MMAs have completed before TMEM is released
+      mma_commit(done);
+      mbar_wait_bounded(done, 0, p.timeout_ns);
+    }
+  } else if ((warp >= kWarpConv0 && warp < kWarpConv0 + 4) || warp >= kWarpConv1) {
+    // -------------------------------------------------------- weights into fp16 A
+    // Thread `lane` of warp q of a set handles row r = 32q + lane of each 128 x 64 A block:
+    // 16-byte loads from the weight ring (64-byte TMA swizzle: chunk c of row r sits at
+    // chunk c ^ ((r >> 1) & 3)), int8 -> fp16 in registers (fp16 outlier weights are
+    // copied as they are), eight 16-byte stores into the 128-byte-swizzled A stage
+    // (chunk c of row r at chunk c ^ (r & 7)).
+    if (!p.debug_skip_loads) {
+      const int set = warp >= kWarpConv1 ? 1 : 0;
+      const int r = 32 * (warp & 3) + lane;
+      const uint32_t swz8 = (uint32_t)(r >> 1) & 3u;
+      const uint32_t swz16 = (uint32_t)r & 7u;
+      uint32_t it = 0, i8 = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+          const bool is_int = kb < p.nkb;
+          const uint32_t i8_0 = i8;
+          i8 += is_int ? 1u : 2u;
+          if ((int)(it & 1u) != set) continue;  // K block `it` belongs to set it & 1
+          const uint32_t s = it % kS, ph = (it / kS) & 1u;
+          // the MMAs that last read A stage s have completed
+          if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
+          uint32_t a[32];
+          if (is_int) {
+            const uint32_t s8 = i8_0 % kS8;
+            if (!(ok = pipe_wait(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
+            const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
+            uint4 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[8];
+              cvt_s8x16_to_f16x16(v[c], o);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) a[8 * c + k] = o[k];
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
+              if (!(ok = pipe_wait(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
+              const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 v = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
+                a[16 * h + 4 * c + 0] = v.x;
+                a[16 * h + 4 * c + 1] = v.y;
+                a[16 * h + 4 * c + 2] = v.z;
+                a[16 * h + 4 * c + 3] = v.w;
+              }
+            }
+            if (!ok) break;
+          }
+          const uint32_t dst = sbase + C::a16 + s * kA16Bytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(dst + (((uint32_t)c ^ swz16) << 4), a[4 * c], a[4 * c + 1],
+                         a[4 * c + 2], a[4 * c + 3]);
+          // each thread orders its shared stores before the tensor core reads them; the
+          // warp then signals once
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&a8_empty[i8_0 % kS8]);
+            if (!is_int) mbar_arrive(&a8_empty[(i8_0 + 1) % kS8]);
+            mbar_arrive(&full_a[s]);
+          }
+        }
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+    // -------------------------------------------------------- epilogue
+    constexpr int kNR = (BN + 31) / 32;  // prefetched row scales per lane
+    const int q = warp & 3;
+    const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+    uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
+    const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+    // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
+    int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
+    uint32_t nseg = 0, slot = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
+      const int m0 = m_blk * BM, n0 = n_blk * BN;
+      const int o = m0 + q * 32 + lane;
+      const bool o_ok = o < p.out;
+      const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
+      const float so = o_ok ? __ldg(&p.scb[o]) * (1.0f / 16129.0f) : 0.0f;
+      float ra[kNR];  // row scales of the tile's tokens, 32 per register, one per lane
+#pragma unroll
+      for (int i = 0; i < kNR; ++i) {
+        const int tk = n0 + 32 * i + lane;
+        ra[i] = tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f;
+      }
+      const int nseg_int = count_int_segments(p, n_blk);
+      const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
+      for (int si = 0; si < nseg_tile && ok; ++si, ++nseg) {
+        const bool is_out = si >= nseg_int;
+        const bool first = si == 0;
+        const bool last = si == nseg_tile - 1;
+        const uint32_t b = nseg & 1u;
+        if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
+        tc_fence_after();
+        const uint32_t tF = tq + b * BN;
+        if (!last) {
+          // an int segment that is not the last one of the tile: fold it into the
+          // running sum (first segment: store it)
+#pragma unroll 1
+          for (int j0 = 0; j0 < BN; j0 += kW) {
+            uint32_t f[kW];
+            tmem_ld<kW>(tF + j0, f);
+            int prev[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) prev[j] = first ? 0 : accs[(size_t)(j0 + j) * 128];
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < kW; ++j)
+              accs[(size_t)(j0 + j) * 128] = prev[j] + __float2int_rn(__uint_as_float(f[j]));
+          }
+          // the accumulator is free as soon as it has been read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tmem_empty[b]);
+        } else {
+#pragma unroll 1
+          for (int j0 = 0; j0 < BN; j0 += kW) {
+            uint32_t f[kW];
+            tmem_ld<kW>(tF + j0, f);
+            int prev[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) prev[j] = first ? 0 : accs[(size_t)(j0 + j) * 128];
+            tmem_ld_wait();
+            if (j0 + kW >= BN) {  // all of F has been read: release it to the MMA
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tmem_empty[b]);
+            }
+            const float ra_s = ra[0];  // this slice's tokens, one per lane
+            uint32_t yh[kW / 2];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+              int acc;
+              float fo = 0.0f;
+              if (is_out) {
+                acc = prev[j];
+                fo = __uint_as_float(f[j]);
+              } else {
+                acc = __float2int_rn(__uint_as_float(f[j])) + prev[j];
+              }
+              const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+              const float y = (float)acc * (rj * so) + fo + bo;
+              const uint32_t h = __half_as_ushort(__float2half_rn(y));
+              yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
+              if constexpr (kDebug) prev[j] = acc;
+            }
+            box_reuse_wait(lane);
+            box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
+                          n0 + j0, lane);
+            slot ^= 1u;
+            if constexpr (kDebug) {
+#pragma unroll 1
+              for (int j = 0; j < kW; ++j) {
+                const int tok = n0 + j0 + j;
+                if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = prev[j];
+              }
+            }
+            if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales
+#pragma unroll
+              for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();  // output stores complete before the CTA exits
+  }
+
+  // -------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int BN, bool kDebug>
+cudaError_t launch_kernel(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
+                          const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
+                          const Params& p, int grid) {
+  using C = Cfg<BN>;
+  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kDebug>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
+  if (e != cudaSuccess) return e;
+  i8_gemm_kernel<BN, kDebug><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
+  using C = Cfg<BN>;
+  CUtensorMap mA8, mB, mWo, mXo, mY;
+  bool ok = true;
+  ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM, BK,
+                 CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= make_map(&mB, a.b_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.in, BN, BK,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  // outlier weights: 128 rows x 32 fp16 (64 bytes) per box, two boxes per K block
+  ok &= make_map(&mWo, a.wout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out, a.ncap, BM, BK / 2,
+                 CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= make_map(&mXo, a.xout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.ncap, BN, BK,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  // Y [T, out] fp16 through TMA stores when its row pitch is a multiple of 16 bytes
+  const bool y_tma = (a.out % 8) == 0;
+  if (y_tma)
+    ok &= make_map(&mY, a.Y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.out, C::kW, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  else
+    mY = mB;  // a valid descriptor that is never used
+  if (!ok) return cudaErrorInvalidValue;
+  Params p{};
+  p.T = a.T;
+  p.in = a.in;
+  p.out = a.out;
+  p.m_tiles = (a.out + BM - 1) / BM;
+  p.n_tiles = (a.T + BN - 1) / BN;
+  p.nkb = (a.in + BK - 1) / BK;
+  p.nchunks = num_chunks(a.in);
+  p.y_tma = y_tma ? 1 : 0;
+  p.hdr = a.hdr;
+  p.rowabs = a.rowabs;
+  p.l1 = a.l1;
+  p.acc_scratch = a.acc_scratch;
+  p.scb = a.scb;
+  p.bias = static_cast<const uint16_t*>(a.bias);
+  p.Y = static_cast<uint16_t*>(a.Y);
+  p.acc_debug = a.acc_debug;
+  p.timeout_ns = a.timeout_ns;
+  p.debug_skip_loads = a.debug_skip_loads;
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < kSmCount ? tiles : kSmCount;
+  if (a.acc_debug) return launch_kernel<BN, true>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  return launch_kernel<BN, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
+}
+
+}  // namespace
+}  // namespace gemm
+
+cudaError_t launch_i8_gemm(const GemmArgs& a, cudaStream_t s) {
+  switch (i8_bn(a.T)) {
+    case 16: return gemm::launch_bn<16>(a, s);
+    case 32: return gemm::launch_bn<32>(a, s);
+    case 64: return gemm::launch_bn<64>(a, s);
+    case 128: return gemm::launch_bn<128>(a, s);
+    default: return gemm::launch_bn<256>(a, s);
+  }
+}
+
+}  // namespace i8mm

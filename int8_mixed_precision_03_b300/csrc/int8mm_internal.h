@@ -13,10 +13,10 @@ constexpr int kKBlock = 64;         // K elements per pipeline stage (128 bytes 
 constexpr int kChunkKBlocks = 16;   // K blocks per exact fp32 accumulation chunk (1024 K)
 constexpr int kChunkK = kKBlock * kChunkKBlocks;
 
-// Token tile (MMA N) of the tensor-core matmul for T tokens: the smallest supported size
-// that covers T, 256 for large T. The quantize pass uses it to group its per-chunk code
-// statistics by token tile.
-inline int gemm_bn(int T) {
+// Token tile (MMA N) of the int8 tensor-core matmul for T tokens: the smallest supported
+// size that covers T, 256 for large T. The quantize pass uses it to group its per-chunk
+// code statistics by token tile.
+inline int i8_bn(int T) {
   return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256;
 }
 inline int num_chunks(int in) { return (in + kChunkK - 1) / kChunkK; }
@@ -35,6 +35,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 // int8_matmul_workspace_size() and int8_matmul().
 struct WsLayout {
   size_t header = 0, mask = 0, l1 = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0;
+  size_t acc = 0;         // int32 running sums of the matmul's epilogue, one tile per SM
   size_t total = 0;
   size_t zero_bytes = 0;  // header + mask + l1: memset at the start of every call
   int words = 0;          // 32-column words of the outlier mask
@@ -52,7 +53,7 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.mask = off; off = align_up(off + sizeof(uint32_t) * L.words, 256);
   // per (token tile, 1024-K chunk): max over the tile's rows of sum |code| in the chunk
   L.l1 = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)((T + gemm_bn(T) - 1) / gemm_bn(T)) *
+  off = align_up(off + sizeof(int32_t) * (size_t)((T + i8_bn(T) - 1) / i8_bn(T)) *
                            num_chunks(in), 256);
   L.zero_bytes = off;
   L.idx = off; off = align_up(off + sizeof(int32_t) * (size_t)in, 256);
@@ -60,6 +61,7 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.rowabs = off; off = align_up(off + 4 * (size_t)T, 256);
   L.xout = off; off = align_up(off + 2 * (size_t)T * ncap, 256);
   L.wout = off; off = align_up(off + 2 * (size_t)out * ncap, 256);
+  L.acc = off; off = align_up(off + 4 * (size_t)kSmCount * 128 * i8_bn(T), 256);
   L.total = off;
   return L;
 }
@@ -94,6 +96,7 @@ struct GemmArgs {
   WsHeader* hdr = nullptr;      // status word + n_out (int8 path), may be null for fp16
   const float* rowabs = nullptr;
   const int32_t* l1 = nullptr;  // per (token tile, chunk) code-magnitude bounds, or null
+  int32_t* acc_scratch = nullptr;  // [kSmCount][BN][128] int32 epilogue running sums
   const float* scb = nullptr;
   const void* bias = nullptr;
   void* Y = nullptr;
@@ -102,6 +105,8 @@ struct GemmArgs {
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)
 };
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+// The int8 path (a_int8 set) and the fp16 comparator (a_f16 set).
+cudaError_t launch_i8_gemm(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_f16_gemm(const GemmArgs& a, cudaStream_t s);
 
 }  // namespace i8mm

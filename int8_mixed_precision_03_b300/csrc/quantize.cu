@@ -261,7 +261,7 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
   quantize_gather_kernel<<<T + wblocks, kRowThreads, smem, s>>>(
       static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,
       static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),
-      static_cast<uint16_t*>(wout), l1, gemm_bn(T), xq8_debug);
+      static_cast<uint16_t*>(wout), l1, i8_bn(T), xq8_debug);
   return cudaGetLastError();
 }
 
