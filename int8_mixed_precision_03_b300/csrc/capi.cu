@@ -100,32 +100,65 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
     return st;
   ++g_last_launches;
   prof_mark(1, s);
-  if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
-                                             ws + L.xq, rowabs, ws + L.xout, ws + L.wout,
-                                             l1, dbg_xq, s))) != I8_OK)
-    return st;
-  ++g_last_launches;
-  prof_mark(2, s);
-  GemmArgs g;
-  g.a_int8 = CB;
-  g.b_f16 = ws + L.xq;
-  g.wout = ws + L.wout;
-  g.xout = ws + L.xout;
-  g.ncap = ncap;
-  g.hdr = hdr;
-  g.rowabs = rowabs;
-  g.l1 = l1;
-  g.acc_scratch = reinterpret_cast<int32_t*>(ws + L.acc);
-  g.scb = SCB;
-  g.bias = bias;
-  g.Y = Y;
-  g.acc_debug = dbg_acc;
-  g.T = T;
-  g.in = in;
-  g.out = out;
-  if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
-  ++g_last_launches;
-  prof_mark(3, s);
+  if (gemv_fits(T, in)) {
+    // decode sizes: int8 codes for the CUDA-core matmul, which reads the outlier weights
+    // from CB itself (no W_out gather)
+    int8_t* xq8 = reinterpret_cast<int8_t*>(ws + L.xq);
+    if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
+                                               nullptr, rowabs, ws + L.xout, nullptr, l1, xq8,
+                                               s))) != I8_OK)
+      return st;
+    ++g_last_launches;
+    prof_mark(2, s);
+    GemvArgs g;
+    g.CB = CB;
+    g.SCB = SCB;
+    g.T = T;
+    g.in = in;
+    g.out = out;
+    g.xq8 = xq8;
+    g.rowabs = rowabs;
+    g.hdr = hdr;
+    g.idx = idx;
+    g.xout = ws + L.xout;
+    g.ncap = ncap;
+    g.bias = bias;
+    g.Y = Y;
+    g.acc_debug = dbg_acc;
+    if ((st = from_cuda(launch_gemv_i8(g, s))) != I8_OK) return st;
+    ++g_last_launches;
+    prof_mark(3, s);
+    if (dbg_xq && cudaMemcpyAsync(dbg_xq, xq8, (size_t)T * in, cudaMemcpyDeviceToDevice, s) !=
+                      cudaSuccess)
+      return I8_ERR_CUDA;
+  } else {
+    if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
+                                               ws + L.xq, rowabs, ws + L.xout, ws + L.wout,
+                                               l1, dbg_xq, s))) != I8_OK)
+      return st;
+    ++g_last_launches;
+    prof_mark(2, s);
+    GemmArgs g;
+    g.a_int8 = CB;
+    g.b_f16 = ws + L.xq;
+    g.wout = ws + L.wout;
+    g.xout = ws + L.xout;
+    g.ncap = ncap;
+    g.hdr = hdr;
+    g.rowabs = rowabs;
+    g.l1 = l1;
+    g.acc_scratch = reinterpret_cast<int32_t*>(ws + L.acc);
+    g.scb = SCB;
+    g.bias = bias;
+    g.Y = Y;
+    g.acc_debug = dbg_acc;
+    g.T = T;
+    g.in = in;
+    g.out = out;
+    if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
+    ++g_last_launches;
+    prof_mark(3, s);
+  }
   // debug copies of the intermediates (stream-ordered device copies)
   if (dbg_idx && cudaMemcpyAsync(dbg_idx, idx, sizeof(int32_t) * (size_t)in,
                                  cudaMemcpyDeviceToDevice, s) != cudaSuccess)

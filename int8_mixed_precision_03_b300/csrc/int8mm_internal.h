@@ -105,6 +105,27 @@ struct GemmArgs {
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)
 };
+// Decode-size int8 matmul on the CUDA cores (T <= kGemvMaxT tokens whose int8 codes fit
+// in shared memory): streams CB at HBM rate with exact int32 dp4a sums.
+constexpr int kGemvMaxT = 8;
+constexpr size_t kGemvMaxSmem = 200 * 1024;
+struct GemvArgs {
+  const int8_t* CB = nullptr;
+  const float* SCB = nullptr;
+  int T = 0, in = 0, out = 0;
+  const int8_t* xq8 = nullptr;    // int8 codes [T, in], outlier columns 0
+  const float* rowabs = nullptr;  // [T]
+  const WsHeader* hdr = nullptr;  // n_out_used
+  const int32_t* idx = nullptr;   // outlier columns
+  const void* xout = nullptr;     // fp16 [T, ncap]
+  int ncap = 0;
+  const void* bias = nullptr;
+  void* Y = nullptr;
+  int32_t* acc_debug = nullptr;
+};
+bool gemv_fits(int T, int in);
+cudaError_t launch_gemv_i8(const GemvArgs& a, cudaStream_t s);
+
 // The int8 path (a_int8 set) and the fp16 comparator (a_f16 set).
 cudaError_t launch_i8_gemm(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_f16_gemm(const GemmArgs& a, cudaStream_t s);

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
     const size_t i = blockIdx.x;
     const uint16_t* x = X + i * in;
     const float a = quantize_row<true>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
-                                       xq16 + i * in, s_red, s_l1);
+                                       xq16 ? xq16 + i * in : nullptr, s_red, s_l1);
     if (threadIdx.x == 0) rowabs[i] = a;
     __syncthreads();
     // bound of the matmul's fp32 chunk sums: max over the token tile of sum |code|
@@ -256,7 +256,9 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
                                    int32_t* l1, int8_t* xq8_debug, cudaStream_t s) {
-  const int wblocks = (out + 31) / 32;
+  // without a W_out buffer (the decode path reads the outlier weights from CB itself) only
+  // the T row blocks run
+  const int wblocks = wout ? (out + 31) / 32 : 0;
   const size_t smem = sizeof(uint32_t) * (size_t)((in + 31) / 32);
   quantize_gather_kernel<<<T + wblocks, kRowThreads, smem, s>>>(
       static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,
