@@ -50,27 +50,40 @@ def load_peaks() -> tuple[dict, str]:
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
-GEMM_SOURCES = [os.path.join(ROOT, "int8_mixed_precision_03_b300", "csrc", f)
-                for f in ("gemm_i8.cu", "gemm_common.cuh", "sm103_ptx.cuh", "int8mm_internal.h")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "int8_mixed_precision_03_b300", "csrc")
+KERNEL_SOURCES = {
+    "i8_gemm_kernel": ("gemm_i8.cu", "gemm_common.cuh", "sm103_ptx.cuh", "int8mm_internal.h"),
+    "gemv_i8_kernel": ("gemv_i8.cu", "int8mm_internal.h"),
+}
+GEMV_MAX_T = 8          # the decode-size CUDA-core kernel handles T <= 8 (codes in smem)
+GEMV_MAX_SMEM = 200 * 1024
 
 
-def gemm_source_hash() -> str:
+def uses_gemv(w: synth.Workload) -> bool:
+    return 1 <= w.T <= GEMV_MAX_T and w.T * w.d_in <= GEMV_MAX_SMEM
+
+
+def matmul_kernel(w: synth.Workload) -> str:
+    return "gemv_i8_kernel" if uses_gemv(w) else "i8_gemm_kernel"
+
+
+def kernel_source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
-        h.update(open(f, "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per GEMM launch from the committed ncu capture, if it was taken on this
-    exact kernel source and workload; None otherwise."""
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the matmul kernel from the committed ncu capture, if it was
+    taken on this exact kernel source and workload; None otherwise."""
     try:
-        rec = json.load(open(TRAFFIC_FILE))
-    except (OSError, ValueError):
+        rec = json.load(open(TRAFFIC_FILE)).get(workload)
+    except (OSError, ValueError, AttributeError):
         return None
-    if rec.get("source_sha256") != gemm_source_hash() or rec.get("workload") != workload:
+    if not rec or rec.get("kernel") != kernel or rec.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -85,35 +98,39 @@ def algorithmic_bytes(w: synth.Workload) -> int:
     return 2 * w.T * w.d_in + w.d_in * w.d_out + 4 * w.d_out + 2 * w.d_out + 2 * w.T * w.d_out
 
 
-def gemm_bytes(w: synth.Workload) -> int:
-    """Algorithmic bytes of the matmul kernel: CB, the fp16 activation codes, SCB, rowabs,
-    bias and Y (the outlier slices are a few KB and are left out)."""
-    return w.d_in * w.d_out + 2 * w.T * w.d_in + 4 * w.d_out + 4 * w.T + 2 * w.d_out \
-        + 2 * w.T * w.d_out
+def matmul_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of the matmul kernel: CB, the activation codes (int8 for the
+    decode kernel, fp16 for the tensor-core kernel), SCB, rowabs, bias and Y (the outlier
+    slices are a few KB and are left out)."""
+    code_bytes = 1 if uses_gemv(w) else 2
+    return (w.d_in * w.d_out + code_bytes * w.T * w.d_in + 4 * w.d_out + 4 * w.T
+            + 2 * w.d_out + 2 * w.T * w.d_out)
 
 
 def hbm_bound(w: synth.Workload) -> bool:
-    """Decode shapes (T <= 64): streaming CB from HBM takes longer than the tensor work."""
+    """Decode shapes (T <= 64): streaming CB from HBM takes longer than the arithmetic."""
     return w.T <= 64
 
 
-def roofline(w: synth.Workload, gemm_ms: float, peaks: dict, peak_src: str) -> dict:
-    """Roofline of the dominant kernel (the tensor-core matmul), from its CUDA-event time."""
-    s = gemm_ms / 1e3
-    traffic = measured_traffic(w.name)
+def roofline(w: synth.Workload, matmul_ms: float, peaks: dict, peak_src: str) -> dict:
+    """Roofline of the dominant kernel (the matmul), from its CUDA-event time."""
+    s = matmul_ms / 1e3
+    kernel = matmul_kernel(w)
+    traffic = measured_traffic(w.name, kernel)
     if hbm_bound(w):
-        achieved = gemm_bytes(w) / s / 1e9
+        achieved = matmul_bytes(w) / s / 1e9
         peak = float(peaks["hbm_gbs"])
+        desc = ("gemv_i8_kernel (dp4a on CUDA cores, int8 codes)" if kernel == "gemv_i8_kernel"
+                else "i8_gemm_kernel (tcgen05 kind::f16 on exact int8 codes), decode tile")
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "algorithmic_bytes": gemm_bytes(w),
-                "kernel": "gemm (tcgen05 kind::f16 on exact int8 codes), decode tile",
+                "algorithmic_bytes": matmul_bytes(w), "kernel": desc,
                 "peak_source": f"hbm_gbs, {peak_src} (MEASURED_PEAKS.json)"}
     achieved = workload_ops(w) / s / 1e12
     peak = float(peaks["bf16_tflops"])
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
-            "kernel": "gemm (tcgen05 kind::f16 on exact int8 codes)",
+            "kernel": "i8_gemm_kernel (tcgen05 kind::f16 on exact int8 codes)",
             "peak_source": f"bf16_tflops burst, {peak_src} (MEASURED_PEAKS.json); the int8 "
                            "product runs on kind::f16, at the bf16/fp16 rate"}
 
@@ -328,7 +345,7 @@ def run_ours(args) -> None:
         flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
         i8.i8_set_profile_events(ev[k])
         step()
-        launches += 3                             # our kernels: colstats, quantize, gemm
+        launches += 3                             # our kernels: colstats, quantize, matmul
         ends[k].record()
     i8.i8_set_profile_events(None)
     torch.cuda.synchronize()
@@ -343,7 +360,7 @@ def run_ours(args) -> None:
     step_ms = [ev[k][0].elapsed_time(ends[k]) for k in range(K)]
     k_ms = {"colstats": [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)],
             "quantize_gather": [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)],
-            "gemm": [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]}
+            "matmul": [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]}
     local_s = sum(step_ms) / 1e3
     ops = workload_ops(w)
     total_s, total_ops = aggregate(local_s, ops * K)
@@ -387,8 +404,7 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    gemm_ms = statistics.mean(k_ms["gemm"])
-    roof = roofline(w, gemm_ms, peaks, peak_src)
+    roof = roofline(w, statistics.mean(k_ms["matmul"]), peaks, peak_src)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_s / K * 1e3, "higher_is_better": True,

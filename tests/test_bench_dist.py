@@ -51,13 +51,24 @@ def test_aggregate_single_process_passthrough():
 def test_traffic_lookup_is_tied_to_the_kernel_source(tmp_path, monkeypatch):
     import json
     import bench
-    rec = {"source_sha256": bench.gemm_source_hash(), "workload": "w",
-           "dram_bytes_per_launch": 123.0}
+    k = "i8_gemm_kernel"
+    rec = {"w": {"kernel": k, "source_sha256": bench.kernel_source_hash(k),
+                 "dram_bytes_per_launch": 123.0}}
     f = tmp_path / "t.json"
     f.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.measured_traffic("w") == 123.0
-    assert bench.measured_traffic("other") is None
-    rec["source_sha256"] = "0" * 64
+    assert bench.measured_traffic("w", k) == 123.0
+    assert bench.measured_traffic("other", k) is None
+    assert bench.measured_traffic("w", "gemv_i8_kernel") is None
+    rec["w"]["source_sha256"] = "0" * 64
     f.write_text(json.dumps(rec))
-    assert bench.measured_traffic("w") is None
+    assert bench.measured_traffic("w", k) is None
+
+
+def test_matmul_path_selection_follows_the_library_rule():
+    import bench
+    import synth
+    assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t1"]) == "gemv_i8_kernel"
+    assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t8"]) == "gemv_i8_kernel"
+    assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t64"]) == "i8_gemm_kernel"
+    assert bench.matmul_kernel(synth.WORKLOADS["ffn_6.7b_up"]) == "i8_gemm_kernel"
