@@ -91,8 +91,10 @@ size_t int8_matmul_workspace_size(int T, int in, int out, int max_outlier_cols);
  *               time must not share a workspace.
  * `in` must be a multiple of 16 and <= I8_MAX_IN; T == 0 or out == 0 is a no-op.
  * Launches: one memset of the workspace header and three kernels (column statistics,
- * row quantize + outlier gather, tensor-core matmul). The outlier count stays on the
- * device; no host synchronization.
+ * row quantize + outlier gather, matmul). The matmul is the tensor-core kernel, or, for
+ * decode sizes (T <= 8 with T*in <= 200 KB), a CUDA-core kernel that streams CB at HBM rate
+ * with exact int32 dp4a sums. The outlier count stays on the device; no host
+ * synchronization.
  */
 i8_status int8_matmul(const void* X, int T, int in, const int8_t* CB, const float* SCB, int out,
                       float threshold, const void* bias, void* Y, void* workspace,
@@ -168,7 +170,8 @@ int i8_last_launch_count(void);
  * which loads this library reserves until the process exits. Sizes whose workspace (with a
  * 64-column outlier capacity) does not fit return I8_ERR_SCRATCH_LIMIT before any launch;
  * within the limit the outlier capacity is the largest multiple of 64 columns that fits.
- * Roughly: 2*T*in + 128*(T + out) + 4*in bytes plus a few KB must fit in 32 MiB.
+ * Roughly: 2*T*in + 128*(T + out) + 4*in + 75776*BN bytes plus a few KB must fit in
+ * 32 MiB, with BN the matmul's token tile (16, 32, 64, 128 or, above 128 tokens, 256).
  * - The first call on a device looks up the scratch's device address (once per device,
  *   with that device current); make that first call before any stream capture.
  * - All calls share the one scratch and it keeps the last call's contents; the parts that
