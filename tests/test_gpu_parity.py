@@ -106,6 +106,20 @@ def test_ragged_shapes(i8, T, d, out, k):
     run_and_compare(i8, X, W, bias, 6.0)
 
 
+@pytest.mark.parametrize("T,d,out,k", [
+    (1, 14336, 3000, 14),     # 176B-like row length, CUDA-core decode kernel
+    (8, 2048, 4100, 70),      # more outlier columns than the decode kernel's 64-column table
+    (5, 1024, 20000, 3),      # many rows per CTA, odd T
+    (8, 32768, 300, 2),       # T * in beyond the decode kernel's shared memory: tensor path
+    (3, 16, 1, 1),            # one output feature, most warps idle
+])
+def test_decode_sizes(i8, T, d, out, k):
+    w = synth.Workload("decode", T, d, out, n_outlier_cols=k, row_frac=1.0, seed=T + d + out)
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    r, ref = run_and_compare(i8, X, W, bias, 6.0)
+    assert r["n_out"] == len(ref["idx"])
+
+
 def test_no_bias_zero_row_and_all_outlier_row(i8):
     w = synth.Workload("edge", 40, 512, 300, n_outlier_cols=6, row_frac=1.0, seed=3)
     X, W = synth.make_x(w), synth.make_w(w)
