@@ -52,7 +52,7 @@ static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact")
 
 template <int BN>
 struct Cfg {
-  static constexpr int kW = BN < 32 ? BN : 32;  // tokens per epilogue slice
+  static constexpr int kW = 16;  // tokens per epilogue slice
   // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring
   static constexpr int kStages = BN == 256 ? 3 : 4;
   static constexpr int kStages8 = BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
@@ -395,20 +395,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
         tc_fence_after();
         const uint32_t tF = tq + b * BN;
+        // Running sums of the tile (not for its first segment): slice j0's are in pc while
+        // the next slice's load into pn, so the L2 latency is paid once per segment.
+        int pn[kW];
+#pragma unroll
+        for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
         if (!last) {
           // an int segment that is not the last one of the tile: fold it into the
           // running sum (first segment: store it)
 #pragma unroll 1
           for (int j0 = 0; j0 < BN; j0 += kW) {
+            int pc[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) pc[j] = pn[j];
+            if (!first && j0 + kW < BN) {
+#pragma unroll
+              for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
+            }
             uint32_t f[kW];
             tmem_ld<kW>(tF + j0, f);
-            int prev[kW];
-#pragma unroll
-            for (int j = 0; j < kW; ++j) prev[j] = first ? 0 : accs[(size_t)(j0 + j) * 128];
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < kW; ++j)
-              accs[(size_t)(j0 + j) * 128] = prev[j] + __float2int_rn(__uint_as_float(f[j]));
+              accs[(size_t)(j0 + j) * 128] = pc[j] + __float2int_rn(__uint_as_float(f[j]));
           }
           // the accumulator is free as soon as it has been read
           tc_fence_before();
@@ -417,11 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll 1
           for (int j0 = 0; j0 < BN; j0 += kW) {
+            int pc[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) pc[j] = pn[j];
+            if (!first && j0 + kW < BN) {
+#pragma unroll
+              for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
+            }
             uint32_t f[kW];
             tmem_ld<kW>(tF + j0, f);
-            int prev[kW];
-#pragma unroll
-            for (int j = 0; j < kW; ++j) prev[j] = first ? 0 : accs[(size_t)(j0 + j) * 128];
             tmem_ld_wait();
             if (j0 + kW >= BN) {  // all of F has been read: release it to the MMA
               tc_fence_before();
@@ -435,16 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               int acc;
               float fo = 0.0f;
               if (is_out) {
-                acc = prev[j];
+                acc = pc[j];
                 fo = __uint_as_float(f[j]);
               } else {
-                acc = __float2int_rn(__uint_as_float(f[j])) + prev[j];
+                acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
               }
               const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
               const float y = (float)acc * (rj * so) + fo + bo;
               const uint32_t h = __half_as_ushort(__float2half_rn(y));
               yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
-              if constexpr (kDebug) prev[j] = acc;
+              if constexpr (kDebug) pc[j] = acc;
             }
             box_reuse_wait(lane);
             box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
               for (int j = 0; j < kW; ++j) {
                 const int tok = n0 + j0 + j;
-                if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = prev[j];
+                if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = pc[j];
               }
             }
             if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales

@@ -46,105 +46,162 @@ __device__ __forceinline__ bool is_masked(const uint32_t* smask, int j) {
   return (smask[j >> 5] >> (j & 31)) & 1u;
 }
 
+// Mask bits of the 8 columns of 16-byte chunk c (bit e <-> column 8c + e).
+__device__ __forceinline__ uint32_t chunk_mask(const uint32_t* smask, int c) {
+  return (smask[c >> 2] >> ((c & 3) * 8)) & 0xffu;
+}
+
+// Max |x| bit pattern of the 8 fp16 values of a chunk (masked columns excluded).
+template <bool kMasked>
+__device__ __forceinline__ uint32_t chunk_absmax(const uint4& v, uint32_t mb) {
+  uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu, v.w & 0x7fff7fffu};
+  if (kMasked) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t keep = ((mb >> (2 * k)) & 1u ? 0u : 0x0000ffffu) |
+                            ((mb >> (2 * k + 1)) & 1u ? 0u : 0xffff0000u);
+      w[k] &= keep;
+    }
+  }
+  uint32_t mx = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+  return mx;
+}
+
+// Codes of the 8 values of chunk c with scale s; writes them to q8 / q16 (either may be
+// null) and returns sum |code|.
+template <bool kMasked>
+__device__ __forceinline__ int chunk_codes(const uint4& v, uint32_t mb, float s, int c,
+                                           int8_t* __restrict__ q8, uint16_t* __restrict__ q16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int q[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    q[2 * k] = absmax_code(h2f(w[k] & 0xffffu), s);
+    q[2 * k + 1] = absmax_code(h2f(w[k] >> 16), s);
+  }
+  if (kMasked) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if ((mb >> e) & 1u) q[e] = 0;
+  }
+  int a1 = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a1 += abs(q[e]);
+  if (q8) {
+    uint2 o;
+    o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
+          ((uint32_t)(q[3] & 0xff) << 24);
+    o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
+          ((uint32_t)(q[7] & 0xff) << 24);
+    reinterpret_cast<uint2*>(q8)[c] = o;
+  }
+  if (q16) {
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      ow[k] = (uint32_t)__half_as_ushort(__int2half_rn(q[2 * k])) |
+              ((uint32_t)__half_as_ushort(__int2half_rn(q[2 * k + 1])) << 16);
+    reinterpret_cast<uint4*>(q16)[c] = o;
+  }
+  return a1;
+}
+
 // Quantizes one row of `cols` fp16 values.
 //   kMasked: columns flagged in smask are excluded from the absmax and coded 0.
 //   q8 (nullable): int8 codes; q16 (nullable): the same codes as exact fp16 values.
 //   s_l1 (nullable, shared, zeroed): += sum of |code| per 1024-column chunk.
 // Returns the row absmax (over unmasked columns).
-template <bool kMasked>
+//
+// kNV > 0: the row is read from memory once and held in registers, thread t owning 16-byte
+// chunks t, t + 256, ..., t + 256 (kNV - 1) (needs cols % 8 == 0, cols <= 2048 kNV).
+// kNV == 0: two passes over the row (any length).
+template <bool kMasked, int kNV>
 __device__ float quantize_row(const uint16_t* __restrict__ x, int cols,
                               const uint32_t* smask, int8_t* __restrict__ q8,
                               uint16_t* __restrict__ q16, uint32_t* s_red,
                               int* s_l1 = nullptr) {
   const int tid = threadIdx.x;
-  const bool vec = (cols & 7) == 0;
-  uint32_t mx = 0;  // running max of |x| bit patterns
-  if (vec) {
+  if constexpr (kNV > 0) {
     const int nch = cols >> 3;
-    for (int c = tid; c < nch; c += kRowThreads) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + c);
-      uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
-                       v.w & 0x7fff7fffu};
-      if (kMasked) {
-        const uint32_t mb = (smask[c >> 2] >> ((c & 3) * 8)) & 0xffu;
+    uint4 v[kNV];
+    uint32_t mx = 0;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t keep = ((mb >> (2 * k)) & 1u ? 0u : 0x0000ffffu) |
-                                ((mb >> (2 * k + 1)) & 1u ? 0u : 0xffff0000u);
-          w[k] &= keep;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      v[i] = c < nch ? __ldg(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0, 0, 0, 0);
+      mx = max(mx, chunk_absmax<kMasked>(v[i], kMasked && c < nch ? chunk_mask(smask, c) : 0u));
     }
-  } else {
-    for (int j = tid; j < cols; j += kRowThreads) {
-      if (kMasked && is_masked(smask, j)) continue;
-      mx = max(mx, (uint32_t)(x[j] & 0x7fffu));
-    }
-  }
-  const float a = h2f((uint16_t)block_max_u32(mx, s_red));
-  const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
-
-  if (vec) {
-    const int nch = cols >> 3;
-    for (int c = tid; c < nch; c += kRowThreads) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const uint32_t mb = kMasked ? (smask[c >> 2] >> ((c & 3) * 8)) & 0xffu : 0u;
-      int q[8];
+    const float a = h2f((uint16_t)block_max_u32(mx, s_red));
+    const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        q[2 * k] = absmax_code(h2f(w[k] & 0xffffu), s);
-        q[2 * k + 1] = absmax_code(h2f(w[k] >> 16), s);
-      }
-      if (kMasked) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if ((mb >> e) & 1u) q[e] = 0;
-      }
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      int a1 = 0;
+      if (c < nch) a1 = chunk_codes<kMasked>(v[i], kMasked ? chunk_mask(smask, c) : 0u, s, c, q8, q16);
       if (s_l1) {
-        int a1 = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a1 += abs(q[e]);
-        atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
-      }
-      if (q8) {
-        uint2 o;
-        o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
-              ((uint32_t)(q[3] & 0xff) << 24);
-        o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
-              ((uint32_t)(q[7] & 0xff) << 24);
-        reinterpret_cast<uint2*>(q8)[c] = o;
-      }
-      if (q16) {
-        uint4 o;
-        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          ow[k] = (uint32_t)__half_as_ushort(__int2half_rn(q[2 * k])) |
-                  ((uint32_t)__half_as_ushort(__int2half_rn(q[2 * k + 1])) << 16);
-        reinterpret_cast<uint4*>(q16)[c] = o;
+        // the warp's 32 chunks (256 columns) lie in one 1024-column chunk
+        a1 = __reduce_add_sync(0xffffffffu, a1);
+        if ((tid & 31) == 0 && a1 > 0) atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
       }
     }
+    return a;
   } else {
-    for (int j = tid; j < cols; j += kRowThreads) {
-      int q = absmax_code(h2f(x[j]), s);
-      if (kMasked && is_masked(smask, j)) q = 0;
-      if (q8) q8[j] = (int8_t)q;
-      if (q16) q16[j] = __half_as_ushort(__int2half_rn(q));
+    const bool vec = (cols & 7) == 0;
+    uint32_t mx = 0;  // running max of |x| bit patterns
+    if (vec) {
+      const int nch = cols >> 3;
+      for (int c = tid; c < nch; c += kRowThreads)
+        mx = max(mx, chunk_absmax<kMasked>(__ldg(reinterpret_cast<const uint4*>(x) + c),
+                                           kMasked ? chunk_mask(smask, c) : 0u));
+    } else {
+      for (int j = tid; j < cols; j += kRowThreads) {
+        if (kMasked && is_masked(smask, j)) continue;
+        mx = max(mx, (uint32_t)(x[j] & 0x7fffu));
+      }
     }
+    const float a = h2f((uint16_t)block_max_u32(mx, s_red));
+    const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
+    if (vec) {
+      const int nch = cols >> 3;
+      for (int c = tid; c < nch; c += kRowThreads) {
+        const int a1 = chunk_codes<kMasked>(__ldg(reinterpret_cast<const uint4*>(x) + c),
+                                            kMasked ? chunk_mask(smask, c) : 0u, s, c, q8, q16);
+        if (s_l1) atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
+      }
+    } else {
+      for (int j = tid; j < cols; j += kRowThreads) {
+        int q = absmax_code(h2f(x[j]), s);
+        if (kMasked && is_masked(smask, j)) q = 0;
+        if (q8) q8[j] = (int8_t)q;
+        if (q16) q16[j] = __half_as_ushort(__int2half_rn(q));
+      }
+    }
+    return a;
   }
-  return a;
+}
+
+// Register chunks per thread for a row of `cols` values: 1, 2, 4 or 8, or 0 when the row
+// is longer than 16384 or not a multiple of 8 (two-pass path; deeper register rows would
+// cost more in occupancy than the second read of the row costs).
+inline int row_nv(int cols) {
+  if (cols % 8 != 0) return 0;
+  const int nch = cols / 8;
+  for (int nv = 1; nv <= 8; nv *= 2)
+    if (nch <= nv * kRowThreads) return nv;
+  return 0;
 }
 
 // Standalone absmax rows; also the weight quantizer (rows = output features).
+template <int kNV>
 __global__ void __launch_bounds__(kRowThreads) absmax_rows_kernel(
     const uint16_t* __restrict__ X, int cols, int8_t* __restrict__ Q, float* __restrict__ amax) {
   __shared__ uint32_t s_red[kRowThreads / 32];
   const size_t row = blockIdx.x;
-  const float a = quantize_row<false>(X + row * cols, cols, nullptr, Q + row * cols, nullptr,
-                                      s_red);
+  const float a = quantize_row<false, kNV>(X + row * cols, cols, nullptr, Q + row * cols,
+                                           nullptr, s_red);
   if (threadIdx.x == 0) amax[row] = a;
 }
 
@@ -152,6 +209,7 @@ __global__ void __launch_bounds__(kRowThreads) absmax_rows_kernel(
 //   blocks [0, T): row i -> fp16 codes (outlier columns 0), rowabs[i], and
 //                  X_out[i, k] = X[i, idx[k]] for k < n, zeros up to a multiple of 64;
 //   blocks [T, ..): 32 output features each -> W_out[o, k] = fp16((CB[o,idx[k]]*SCB[o])/127).
+template <int kNV>
 __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
     const uint16_t* __restrict__ X, int T, int in, const int8_t* __restrict__ CB,
     const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
@@ -171,8 +229,8 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
     __syncthreads();
     const size_t i = blockIdx.x;
     const uint16_t* x = X + i * in;
-    const float a = quantize_row<true>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
-                                       xq16 ? xq16 + i * in : nullptr, s_red, s_l1);
+    const float a = quantize_row<true, kNV>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
+                                            xq16 ? xq16 + i * in : nullptr, s_red, s_l1);
     if (threadIdx.x == 0) rowabs[i] = a;
     __syncthreads();
     // bound of the matmul's fp32 chunk sums: max over the token tile of sum |code|
@@ -196,7 +254,14 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
   }
 }
 
+__device__ __forceinline__ int zp_code(float x, float sc, float z) {
+  return max(-127, min(127, __float2int_rn(__fsub_rn(__fmul_rn(x, sc), z))));
+}
+
 // Zeropoint rows: S = 254/(max-min), Z = rint(S*min) + 127, code = clamp(rint(x*S - Z)).
+// kNV > 0: the row is read once and held in registers (as in quantize_row); kNV == 0:
+// element by element, two passes.
+template <int kNV>
 __global__ void __launch_bounds__(kRowThreads) zeropoint_rows_kernel(
     const uint16_t* __restrict__ X, int cols, int8_t* __restrict__ Q, float* __restrict__ S,
     float* __restrict__ Z) {
@@ -204,18 +269,38 @@ __global__ void __launch_bounds__(kRowThreads) zeropoint_rows_kernel(
   const size_t row = blockIdx.x;
   const uint16_t* x = X + row * cols;
   int8_t* q = Q + row * cols;
+  const int tid = threadIdx.x;
   float mn = INFINITY, mx = -INFINITY;
-  for (int j = threadIdx.x; j < cols; j += kRowThreads) {
-    const float v = h2f(x[j]);
-    mn = fminf(mn, v);
-    mx = fmaxf(mx, v);
+  [[maybe_unused]] uint4 v[kNV > 0 ? kNV : 1];
+  if constexpr (kNV > 0) {
+    const int nch = cols >> 3;
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      if (c < nch) {
+        v[i] = __ldg(reinterpret_cast<const uint4*>(x) + c);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = h2f(w[k] & 0xffffu), hi = h2f(w[k] >> 16);
+          mn = fminf(mn, fminf(lo, hi));
+          mx = fmaxf(mx, fmaxf(lo, hi));
+        }
+      }
+    }
+  } else {
+    for (int j = tid; j < cols; j += kRowThreads) {
+      const float xv = h2f(x[j]);
+      mn = fminf(mn, xv);
+      mx = fmaxf(mx, xv);
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = tid & 31, warp = tid >> 5;
   if (lane == 0) { s_mn[warp] = mn; s_mx[warp] = mx; }
   __syncthreads();
   mn = s_mn[0];
@@ -223,31 +308,64 @@ __global__ void __launch_bounds__(kRowThreads) zeropoint_rows_kernel(
 #pragma unroll
   for (int w = 1; w < kRowThreads / 32; ++w) { mn = fminf(mn, s_mn[w]); mx = fmaxf(mx, s_mx[w]); }
   if (cols == 0) { mn = 0.0f; mx = 0.0f; }
-  if (mx > mn) {
-    const float sc = __fdiv_rn(254.0f, __fsub_rn(mx, mn));
-    const float z = __fadd_rn(rintf(__fmul_rn(sc, mn)), 127.0f);
-    if (threadIdx.x == 0) { S[row] = sc; Z[row] = z; }
-    for (int j = threadIdx.x; j < cols; j += kRowThreads) {
-      const int c = __float2int_rn(__fsub_rn(__fmul_rn(h2f(x[j]), sc), z));
-      q[j] = (int8_t)max(-127, min(127, c));
+  const bool spread = mx > mn;
+  const float sc = spread ? __fdiv_rn(254.0f, __fsub_rn(mx, mn)) : 0.0f;
+  const float z = spread ? __fadd_rn(rintf(__fmul_rn(sc, mn)), 127.0f) : mn;
+  if (tid == 0) { S[row] = sc; Z[row] = z; }
+  if constexpr (kNV > 0) {
+    const int nch = cols >> 3;
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      if (c < nch) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        int cq[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          cq[2 * k] = spread ? zp_code(h2f(w[k] & 0xffffu), sc, z) : 0;
+          cq[2 * k + 1] = spread ? zp_code(h2f(w[k] >> 16), sc, z) : 0;
+        }
+        uint2 o;
+        o.x = (cq[0] & 0xff) | ((cq[1] & 0xff) << 8) | ((cq[2] & 0xff) << 16) |
+              ((uint32_t)(cq[3] & 0xff) << 24);
+        o.y = (cq[4] & 0xff) | ((cq[5] & 0xff) << 8) | ((cq[6] & 0xff) << 16) |
+              ((uint32_t)(cq[7] & 0xff) << 24);
+        reinterpret_cast<uint2*>(q)[c] = o;
+      }
     }
   } else {
-    if (threadIdx.x == 0) { S[row] = 0.0f; Z[row] = mn; }
-    for (int j = threadIdx.x; j < cols; j += kRowThreads) q[j] = 0;
+    for (int j = tid; j < cols; j += kRowThreads)
+      q[j] = spread ? (int8_t)zp_code(h2f(x[j]), sc, z) : (int8_t)0;
   }
 }
 
+// Instantiates F<kNV> for the register depth that fits `cols` (0: two-pass path).
+#define I8_DISPATCH_NV(cols, F)                      \
+  switch (row_nv(cols)) {                            \
+    case 1: F(1); break;                             \
+    case 2: F(2); break;                             \
+    case 4: F(4); break;                             \
+    case 8: F(8); break;                             \
+    default: F(0); break;                            \
+  }
+
 cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
                                cudaStream_t s) {
-  absmax_rows_kernel<<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), cols, Q,
-                                                   absmax);
+#define I8_LAUNCH(NV)                                                                    \
+  absmax_rows_kernel<NV><<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), cols, \
+                                                       Q, absmax)
+  I8_DISPATCH_NV(cols, I8_LAUNCH)
+#undef I8_LAUNCH
   return cudaGetLastError();
 }
 
 cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
                                   float* Z, cudaStream_t s) {
-  zeropoint_rows_kernel<<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), cols, Q,
-                                                      S, Z);
+#define I8_LAUNCH(NV)                                                                    \
+  zeropoint_rows_kernel<NV><<<rows, kRowThreads, 0, s>>>(static_cast<const uint16_t*>(X), \
+                                                          cols, Q, S, Z)
+  I8_DISPATCH_NV(cols, I8_LAUNCH)
+#undef I8_LAUNCH
   return cudaGetLastError();
 }
 
@@ -260,10 +378,13 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
   // the T row blocks run
   const int wblocks = wout ? (out + 31) / 32 : 0;
   const size_t smem = sizeof(uint32_t) * (size_t)((in + 31) / 32);
-  quantize_gather_kernel<<<T + wblocks, kRowThreads, smem, s>>>(
-      static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,
-      static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),
-      static_cast<uint16_t*>(wout), l1, i8_bn(T), xq8_debug);
+#define I8_LAUNCH(NV)                                                                       \
+  quantize_gather_kernel<NV><<<T + wblocks, kRowThreads, smem, s>>>(                         \
+      static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,           \
+      static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),                   \
+      static_cast<uint16_t*>(wout), l1, i8_bn(T), xq8_debug)
+  I8_DISPATCH_NV(in, I8_LAUNCH)
+#undef I8_LAUNCH
   return cudaGetLastError();
 }
 
