@@ -329,9 +329,11 @@ def run_ours(args) -> None:
         raise RuntimeError(f"device status {i8.i8_get_status(ws)} after warm-up")
 
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # per-step events around the whole step, plus events between the three kernels (the
+    # roofline's kernel time comes from the same timed region)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for e in starts + ends:   # create the CUDA events before timing
+    for e in [x for row in ev for x in row] + ends:   # create the CUDA events before timing
         e.record()
     torch.cuda.synchronize()
     clocks = ClockSampler(local) if rank == 0 else None
@@ -343,10 +345,11 @@ def run_ours(args) -> None:
     launches = 0
     for k in range(K):
         flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
-        starts[k].record()
+        i8.i8_set_profile_events(ev[k])
         step()
         launches += 3                             # our kernels: colstats, quantize, matmul
         ends[k].record()
+    i8.i8_set_profile_events(None)
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_end()
@@ -355,24 +358,10 @@ def run_ours(args) -> None:
     clk = clocks.stop() if clocks else None
     if i8.i8_get_status(ws) != 0:
         raise RuntimeError(f"device status {i8.i8_get_status(ws)} in the timed region")
-    step_ms = [starts[k].elapsed_time(ends[k]) for k in range(K)]
-
-    # per-kernel breakdown: a second, separately profiled pass (events between the kernels)
-    Kp = min(K, 100)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kp)]
-    for e in [x for row in ev for x in row]:
-        e.record()
-    torch.cuda.synchronize()
-    for k in range(Kp):
-        flush.fill_(k & 0xff)
-        i8.i8_set_profile_events(ev[k])
-        step()
-    i8.i8_set_profile_events(None)
-    torch.cuda.synchronize()
-    prof_step_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][3]) for k in range(Kp))
-    k_ms = {"colstats": [ev[k][0].elapsed_time(ev[k][1]) for k in range(Kp)],
-            "quantize_gather": [ev[k][1].elapsed_time(ev[k][2]) for k in range(Kp)],
-            "matmul": [ev[k][2].elapsed_time(ev[k][3]) for k in range(Kp)]}
+    step_ms = [ev[k][0].elapsed_time(ends[k]) for k in range(K)]
+    k_ms = {"colstats": [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)],
+            "quantize_gather": [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)],
+            "matmul": [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]}
     local_s = sum(step_ms) / 1e3
     ops = workload_ops(w)
     total_s, total_ops = aggregate(local_s, ops * K)
@@ -445,7 +434,6 @@ def run_ours(args) -> None:
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write, untimed)"},
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
-        "profiled_step_us": round(prof_step_ms * 1e3, 2),
         "roofline": roof,
         "e2e": {"value": e2e_ops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(Xpin.numel() * 2),
