@@ -55,17 +55,26 @@ CSRC = os.path.join(ROOT, "int8_mixed_precision_03_b300", "csrc")
 KERNEL_SOURCES = {
     "i8_gemm_kernel": ("gemm_i8.cu", "gemm_common.cuh", "sm103_ptx.cuh", "int8mm_internal.h"),
     "gemv_i8_kernel": ("gemv_i8.cu", "int8mm_internal.h"),
+    "gemv_mma_kernel": ("gemv_mma.cu", "int8mm_internal.h"),
 }
-GEMV_MAX_T = 8          # the decode-size CUDA-core kernel handles T <= 8 (codes in smem)
-GEMV_MAX_SMEM = 200 * 1024
+# decode-size kernels (the library's rule): T <= 8 on dp4a with the int8 codes in shared
+# memory, 9 <= T <= 16 on mma.sync with 128-byte-padded code rows
+GEMV_MAX_T, GEMV_MMA_MIN_T, GEMV_MAX_SMEM = 16, 9, 200 * 1024
 
 
 def uses_gemv(w: synth.Workload) -> bool:
-    return 1 <= w.T <= GEMV_MAX_T and w.T * w.d_in <= GEMV_MAX_SMEM
+    if w.T < 1 or w.T > GEMV_MAX_T:
+        return False
+    if w.T >= GEMV_MMA_MIN_T:
+        xs = (w.d_in + 127) // 128 * 128 + 64
+        return w.T * xs <= GEMV_MAX_SMEM
+    return w.T * w.d_in <= GEMV_MAX_SMEM
 
 
 def matmul_kernel(w: synth.Workload) -> str:
-    return "gemv_i8_kernel" if uses_gemv(w) else "i8_gemm_kernel"
+    if not uses_gemv(w):
+        return "i8_gemm_kernel"
+    return "gemv_mma_kernel" if w.T >= GEMV_MMA_MIN_T else "gemv_i8_kernel"
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -120,8 +129,10 @@ def roofline(w: synth.Workload, matmul_ms: float, peaks: dict, peak_src: str) ->
     if hbm_bound(w):
         achieved = matmul_bytes(w) / s / 1e9
         peak = float(peaks["hbm_gbs"])
-        desc = ("gemv_i8_kernel (dp4a on CUDA cores, int8 codes)" if kernel == "gemv_i8_kernel"
-                else "i8_gemm_kernel (tcgen05 kind::f16 on exact int8 codes), decode tile")
+        desc = {"gemv_i8_kernel": "gemv_i8_kernel (dp4a on CUDA cores, int8 codes)",
+                "gemv_mma_kernel": "gemv_mma_kernel (mma.sync m16n8k16 fp16 on exact int8 codes)",
+                "i8_gemm_kernel": "i8_gemm_kernel (tcgen05 kind::f16 on exact int8 codes), "
+                                  "decode tile"}[kernel]
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": matmul_bytes(w), "kernel": desc,

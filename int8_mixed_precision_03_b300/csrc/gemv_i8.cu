@@ -193,9 +193,13 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool gemv_fits(int T, int in) { return T >= 1 && T <= kGemvMaxT && (size_t)T * in <= kGemvMaxSmem; }
+bool gemv_fits(int T, int in) {
+  if (T >= kGemvMmaMinT) return gemv_mma_fits(T, in);
+  return T >= 1 && (size_t)T * in <= kGemvMaxSmem;
+}
 
 cudaError_t launch_gemv_i8(const GemvArgs& a, cudaStream_t s) {
+  if (a.T >= kGemvMmaMinT) return launch_gemv_mma(a, s);
   switch (a.T) {
     case 1: return launch_t<1>(a, s);
     case 2: return launch_t<2>(a, s);

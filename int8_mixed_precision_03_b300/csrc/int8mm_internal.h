@@ -105,9 +105,11 @@ struct GemmArgs {
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)
 };
-// Decode-size int8 matmul on the CUDA cores (T <= kGemvMaxT tokens whose int8 codes fit
-// in shared memory): streams CB at HBM rate with exact int32 dp4a sums.
-constexpr int kGemvMaxT = 8;
+// Decode-size int8 matmuls (T <= kGemvMaxT tokens whose int8 codes fit in shared memory),
+// streaming CB at HBM rate: exact int32 dp4a sums on the CUDA cores for T < kGemvMmaMinT,
+// mma.sync m16n8k16 (fp16, exact fp32 fragments drained to int32) from kGemvMmaMinT on.
+constexpr int kGemvMaxT = 16;
+constexpr int kGemvMmaMinT = 9;  // below: dp4a (measured faster at T = 8 on B300)
 constexpr size_t kGemvMaxSmem = 200 * 1024;
 struct GemvArgs {
   const int8_t* CB = nullptr;
@@ -123,8 +125,10 @@ struct GemvArgs {
   void* Y = nullptr;
   int32_t* acc_debug = nullptr;
 };
-bool gemv_fits(int T, int in);
-cudaError_t launch_gemv_i8(const GemvArgs& a, cudaStream_t s);
+bool gemv_fits(int T, int in);                            // either decode kernel applies
+cudaError_t launch_gemv_i8(const GemvArgs& a, cudaStream_t s);  // dispatches on T
+bool gemv_mma_fits(int T, int in);
+cudaError_t launch_gemv_mma(const GemvArgs& a, cudaStream_t s);
 
 // The int8 path (a_int8 set) and the fp16 comparator (a_f16 set).
 cudaError_t launch_i8_gemm(const GemmArgs& a, cudaStream_t s);

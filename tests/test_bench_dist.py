@@ -70,5 +70,6 @@ def test_matmul_path_selection_follows_the_library_rule():
     import synth
     assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t1"]) == "gemv_i8_kernel"
     assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t8"]) == "gemv_i8_kernel"
+    assert bench.matmul_kernel(synth.WORKLOADS["tiny"]) == "gemv_mma_kernel"
     assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t64"]) == "i8_gemm_kernel"
     assert bench.matmul_kernel(synth.WORKLOADS["ffn_6.7b_up"]) == "i8_gemm_kernel"

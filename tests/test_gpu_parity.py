@@ -112,6 +112,11 @@ def test_ragged_shapes(i8, T, d, out, k):
     (5, 1024, 20000, 3),      # many rows per CTA, odd T
     (8, 32768, 300, 2),       # T * in beyond the decode kernel's shared memory: tensor path
     (3, 16, 1, 1),            # one output feature, most warps idle
+    (6, 14336, 2000, 14),     # dp4a decode kernel, 176B-like rows
+    (9, 1040, 777, 20),       # mma.sync decode kernel, second token tile, K % 64 != 0
+    (12, 4096, 3000, 70),     # outlier columns beyond the mma.sync kernel's table
+    (16, 8192, 1000, 5),      # the largest decode tile
+    (16, 14336, 500, 3),      # codes too large for shared memory: tensor path
 ])
 def test_decode_sizes(i8, T, d, out, k):
     w = synth.Workload("decode", T, d, out, n_outlier_cols=k, row_frac=1.0, seed=T + d + out)
