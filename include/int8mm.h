@@ -148,6 +148,19 @@ i8_status f16_matmul(const void* X, int T, int in, const void* W, int out, const
  */
 i8_status i8_get_status(const void* workspace, void* stream);
 
+/*
+ * Test hook for the failure path of the tensor-core matmul (T > 16 tokens, or codes too
+ * large for the decode kernels): runs int8_matmul (threshold 6, no bias) but the matmul's
+ * loaders load nothing, so every pipeline wait gives up after wait_limit_ns; the kernel then
+ * records I8_ERR_TIMEOUT in the workspace status word, frees its tensor memory and returns,
+ * and the context stays usable. Read the status with i8_get_status. Y is left undefined.
+ * Returns I8_ERR_INVALID_ARG for decode sizes or wait_limit_ns == 0. No counterpart in the
+ * pages.
+ */
+i8_status i8_test_stalled_matmul(const void* X, int T, int in, const int8_t* CB,
+                                 const float* SCB, int out, void* Y, void* workspace,
+                                 size_t ws_bytes, uint64_t wait_limit_ns, void* stream);
+
 /* Static description of a status code. */
 const char* i8_status_string(i8_status s);
 

@@ -32,6 +32,7 @@ SIGNATURES = {
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
     "zeropoint_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p, _p]),
     "f16_matmul": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
+    "i8_test_stalled_matmul": (_i, [_p, _i, _i, _p, _p, _i, _p, _p, _sz, C.c_uint64, _p]),
     "i8_get_status": (_i, [_p, _p]),
     "i8_status_string": (C.c_char_p, [_i]),
     "i8_last_launch_count": (_i, []),

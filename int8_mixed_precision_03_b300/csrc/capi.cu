@@ -71,10 +71,12 @@ i8_status validate_matmul(const void* X, int T, int in, const int8_t* CB, const 
 i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float* SCB, int out,
                      float threshold, const void* bias, void* Y, void* workspace,
                      size_t ws_bytes, void* stream, int32_t* dbg_idx, int32_t* dbg_n,
-                     int8_t* dbg_xq, float* dbg_rowabs, int32_t* dbg_acc) {
+                     int8_t* dbg_xq, float* dbg_rowabs, int32_t* dbg_acc,
+                     uint64_t stall_ns = 0) {
   g_last_launches = 0;
   i8_status st = validate_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, workspace);
   if (st != I8_OK) return st;
+  if (stall_ns && gemv_fits(T, in)) return I8_ERR_INVALID_ARG;  // a tensor-core-path hook
   if ((dbg_idx && !aligned16(dbg_idx)) || (dbg_n && !aligned16(dbg_n)) ||
       (dbg_xq && !aligned16(dbg_xq)) || (dbg_rowabs && !aligned16(dbg_rowabs)) ||
       (dbg_acc && !aligned16(dbg_acc)))
@@ -155,6 +157,10 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
     g.T = T;
     g.in = in;
     g.out = out;
+    if (stall_ns) {  // test hook: nothing is loaded, so every pipeline wait runs out
+      g.debug_skip_loads = 1;
+      g.timeout_ns = stall_ns;
+    }
     if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
     ++g_last_launches;
     prof_mark(3, s);
@@ -211,6 +217,14 @@ I8_API i8_status int8_matmul_debug(const void* X, int T, int in, const int8_t* C
                                    float* rowabs, int32_t* acc_s32) {
   return run_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, workspace, ws_bytes, stream,
                     outlier_idx, n_out, Xq, rowabs, acc_s32);
+}
+
+I8_API i8_status i8_test_stalled_matmul(const void* X, int T, int in, const int8_t* CB,
+                                        const float* SCB, int out, void* Y, void* workspace,
+                                        size_t ws_bytes, uint64_t wait_limit_ns, void* stream) {
+  if (wait_limit_ns == 0) return I8_ERR_INVALID_ARG;
+  return run_matmul(X, T, in, CB, SCB, out, 6.0f, nullptr, Y, workspace, ws_bytes, stream,
+                    nullptr, nullptr, nullptr, nullptr, nullptr, wait_limit_ns);
 }
 
 I8_API i8_status absmax_quantize_rows(const void* X, int rows, int cols, int8_t* Q,

@@ -114,3 +114,12 @@ def test_other_entry_points_validate(L):
     assert L.f16_matmul(fake(A), 4, 20, fake(A), 8, None, fake(A), None) == 2
     assert L.f16_matmul(fake(A), 0, 32, fake(A), 8, None, fake(A), None) == 0
     assert L.i8_get_status(None, None) == 1
+
+
+def test_stall_hook_rejects_decode_sizes_and_a_zero_limit_before_any_launch():
+    L = i8.lib()
+    p = C.c_void_p(1 << 20)
+    # 8 tokens fit the decode kernels, which the hook does not cover
+    assert L.i8_test_stalled_matmul(p, 8, 256, p, p, 64, p, p, 1 << 30, 1000, None) == 1
+    assert L.i8_test_stalled_matmul(p, 64, 256, p, p, 64, p, p, 1 << 30, 0, None) == 1
+    assert L.i8_last_launch_count() == 0

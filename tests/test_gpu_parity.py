@@ -4,6 +4,7 @@ Bit-exact: outlier column sets, int8 codes, row absmax, CB/SCB, int32 accumulato
 zeropoint codes/S/Z. Floating point: |y - y_ref| <= 2e-2 + 2e-3 |y_ref| for the fp16 output
 against the oracle's fp64 evaluation of the same quantized definition.
 """
+import ctypes as C
 import functools
 import math
 
@@ -259,3 +260,21 @@ def test_full_size_config_sampled_rows(i8, name):
     planted = synth.outlier_columns(w)
     if w.threshold == 6.0:
         assert set(planted.tolist()) <= set(ref["idx"].tolist())
+
+
+def test_stalled_matmul_times_out_and_the_context_stays_usable(i8):
+    """Every pipeline wait of the tensor-core matmul runs out (its loaders load nothing):
+    the kernel records I8_ERR_TIMEOUT and returns; the next call on the stream is correct."""
+    w = synth.Workload("stall", 64, 256, 256, n_outlier_cols=2, seed=5)
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    Xd = dev(X)
+    CB, SCB = i8.int8_quantize_weight(dev(W))
+    ws = i8.alloc_workspace(w.T, w.d_in, w.d_out, "cuda")
+    Y = torch.empty((w.T, w.d_out), dtype=torch.float16, device="cuda")
+    ptr = lambda t: C.c_void_p(t.data_ptr())  # noqa: E731
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = i8.lib().i8_test_stalled_matmul(ptr(Xd), w.T, w.d_in, ptr(CB), ptr(SCB), w.d_out,
+                                         ptr(Y), ptr(ws), ws.numel(), 20_000_000, stream)
+    assert rc == 0
+    assert i8.i8_get_status(ws) == 7  # I8_ERR_TIMEOUT
+    run_and_compare(i8, X, W, bias, 6.0)
