@@ -11,9 +11,11 @@
 // whole call. Warp w of the grid owns the rows [w*out/W, (w+1)*out/W) and walks them four
 // at a time; per step lane l reads bytes [16*(32*v + l), +16) of each of the four rows and
 // the same bytes of every token's codes, so a step covers 512 bytes of K per row. A
-// rolling register pipeline keeps two to four steps of weight loads in flight per warp. After the K loop a butterfly sum leaves
-// every lane with all 4*T dot products; lane (r, t) = (l / 8, l % 8) finishes output
-// feature o = row r of the group for token t:
+// rolling register pipeline keeps four steps of weight loads in flight per warp, and the
+// next group's first loads go out before a group's sums are reduced. The reduction gives
+// lane (r, t) = (l / 8, l % 8) the warp sum of row r, token t (a reduce-scatter for T = 8,
+// a butterfly otherwise), and that lane finishes output feature o = row r of the group for
+// token t:
 //   Y[t, o] = fp16( acc * rowabs[t] * SCB[o]/127^2 + sum_k X_out[t,k] * W_out[o,k] + bias[o] )
 // with W_out[o,k] = fp16(CB[o, idx_k] * SCB[o] / 127), in the same fp32 expressions as
 // the tensor-core path. The outlier bytes CB[o, idx_k] of the CTA's rows (for the first
@@ -29,8 +31,14 @@ namespace {
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) / 16 * 16; }
 
-constexpr int kGvThreads = 512;
-constexpr int kGvWarps = kGvThreads / 32;
+// Threads per CTA and weight-load steps in flight per warp: 512 threads with 4 steps for
+// T <= 2; 384 threads with 4 steps (the registers of 8 tokens' sums) from T = 3 (timed on
+// B300: 2-4 % faster at T = 8 than 512 threads with 2 steps).
+template <int T> struct GvShape {
+  static constexpr int kThreads = T <= 2 ? 512 : 384;
+  static constexpr int kWarps = kThreads / 32;
+  static constexpr int kBuf = 4;
+};
 constexpr int kGvRows = 4;     // rows of CB per warp step
 constexpr int kOutTab = 64;    // outlier columns held in the shared-memory table
 
@@ -59,7 +67,7 @@ __device__ __forceinline__ void dot_step(int (&acc)[kGvRows][T], const uint4 (&w
 }
 
 template <int T>
-__global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
+__global__ void __launch_bounds__(GvShape<T>::kThreads, 1) gemv_i8_kernel(
     const int8_t* __restrict__ CB, const float* __restrict__ SCB, int in, int out,
     const int8_t* __restrict__ xq, const float* __restrict__ rowabs,
     const WsHeader* __restrict__ hdr, const int32_t* __restrict__ idx,
@@ -67,6 +75,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
     uint16_t* __restrict__ Y, int32_t* __restrict__ acc_debug, int use_tab) {
   // shared memory: x codes [T][in] | outlier bytes [rows of this CTA][kOutTab] |
   //                X_out [T][kOutTab] fp32
+  constexpr int kGvThreads = GvShape<T>::kThreads, kGvWarps = GvShape<T>::kWarps;
+  constexpr int kBuf = GvShape<T>::kBuf;
   extern __shared__ uint4 sx[];
   const int nvec = in / 16;  // in % 16 == 0
   const long long W = (long long)gridDim.x * kGvWarps;
@@ -77,6 +87,38 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
   const int n_out = *reinterpret_cast<volatile const int*>(&hdr->n_out_used);
   const int n_tab = min(n_out, use_tab ? kOutTab : 0);
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * kGvWarps + warp;
+  const int r_begin = (int)(gw * out / W), r_end = (int)((gw + 1) * out / W);
+  const int lr = lane / 8, lt = lane % 8;  // the (row, token) this lane finishes
+  const float ra_l = lt < T ? __ldg(&rowabs[lt]) : 0.0f;
+
+  // weight rows of group r0 (rows past the warp's range re-read its last row)
+  auto group_rows = [&](int r0, const uint4* (&wrow)[kGvRows]) {
+    const int nr = min(kGvRows, r_end - r0);
+#pragma unroll
+    for (int r = 0; r < kGvRows; ++r)
+      wrow[r] = reinterpret_cast<const uint4*>(CB + (size_t)(r0 + min(r, nr - 1)) * in);
+  };
+  // rolling pipeline of kBuf steps: a buffer is reloaded right after it is consumed; the
+  // next group's first steps are issued before this group's sums are reduced and finished
+  uint4 w[kBuf][kGvRows];
+  auto load_first = [&](const uint4* (&wrow)[kGvRows]) {
+#pragma unroll
+    for (int bi = 0; bi < kBuf; ++bi) {
+      const int vb = lane + 32 * bi;
+      if (vb < nvec) {
+#pragma unroll
+        for (int r = 0; r < kGvRows; ++r) w[bi][r] = ld_stream16(wrow[r] + vb);
+      }
+    }
+  };
+  const uint4* wrow[kGvRows];
+  if (r_begin < r_end) {
+    group_rows(r_begin, wrow);
+    load_first(wrow);
+  }
+  // shared-memory staging overlaps the first weight loads
   for (int i = threadIdx.x; i < T * nvec; i += kGvThreads)
     sx[i] = __ldg(reinterpret_cast<const uint4*>(xq) + i);
   for (int i = threadIdx.x; i < (cta_r1 - cta_r0) * n_tab; i += kGvThreads) {
@@ -89,12 +131,6 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long gw = (long long)blockIdx.x * kGvWarps + warp;
-  const int r_begin = (int)(gw * out / W), r_end = (int)((gw + 1) * out / W);
-  const int lr = lane / 8, lt = lane % 8;  // the (row, token) this lane finishes
-  const float ra_l = lt < T ? __ldg(&rowabs[lt]) : 0.0f;
-
   for (int r0 = r_begin; r0 < r_end; r0 += kGvRows) {
     const int nr = min(kGvRows, r_end - r0);
     int acc[kGvRows][T];
@@ -102,22 +138,6 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
     for (int r = 0; r < kGvRows; ++r)
 #pragma unroll
       for (int t = 0; t < T; ++t) acc[r][t] = 0;
-    const uint4* wrow[kGvRows];
-#pragma unroll
-    for (int r = 0; r < kGvRows; ++r)  // rows past the warp's range re-read its last row
-      wrow[r] = reinterpret_cast<const uint4*>(CB + (size_t)(r0 + min(r, nr - 1)) * in);
-
-    // rolling pipeline of kBuf steps: a buffer is reloaded right after it is consumed
-    constexpr int kBuf = T <= 2 ? 4 : 2;
-    uint4 w[kBuf][kGvRows];
-#pragma unroll
-    for (int bi = 0; bi < kBuf; ++bi) {
-      const int vb = lane + 32 * bi;
-      if (vb < nvec) {
-#pragma unroll
-        for (int r = 0; r < kGvRows; ++r) w[bi][r] = ld_stream16(wrow[r] + vb);
-      }
-    }
     for (int v = lane; v < nvec; v += 32 * kBuf) {
 #pragma unroll
       for (int bi = 0; bi < kBuf; ++bi) {
@@ -130,20 +150,46 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_i8_kernel(
         }
       }
     }
-    // every lane gets every total
+    if (r0 + kGvRows < r_end) {  // the next group's loads go out now
+      group_rows(r0 + kGvRows, wrow);
+      load_first(wrow);
+    }
+    int a = 0;  // this lane's total: (row, token) = (lane / 8, lane % 8)
+    if constexpr (kGvRows * T == 32) {
+      // reduce-scatter: each round halves the values a lane holds, exchanging the other
+      // half with the partner lane, until lane l holds the warp sum of value l
+      int v[32];
 #pragma unroll
-    for (int r = 0; r < kGvRows; ++r)
+      for (int r = 0; r < kGvRows; ++r)
 #pragma unroll
-      for (int t = 0; t < T; ++t)
+        for (int t = 0; t < T; ++t) v[r * T + t] = acc[r][t];
 #pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], d);
-
-    int a = 0;  // this lane's total, selected without dynamic register indexing
+      for (int wd = 16; wd >= 1; wd >>= 1) {
+        const bool upper = (lane & wd) != 0;
 #pragma unroll
-    for (int r = 0; r < kGvRows; ++r)
+        for (int i = 0; i < wd; ++i) {
+          const int send = upper ? v[i] : v[i + wd];
+          const int keep = upper ? v[i + wd] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, wd);
+        }
+      }
+      a = v[0];
+    } else {
+      // every lane gets every total
 #pragma unroll
-      for (int t = 0; t < T; ++t)
-        if (r == lr && t == lt) a = acc[r][t];
+      for (int r = 0; r < kGvRows; ++r)
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+#pragma unroll
+          for (int d = 16; d >= 1; d >>= 1)
+            acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], d);
+      // select without dynamic register indexing
+#pragma unroll
+      for (int r = 0; r < kGvRows; ++r)
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+          if (r == lr && t == lt) a = acc[r][t];
+    }
     if (lt < T && lr < nr) {
       const int o = r0 + lr;
       const float scb = __ldg(&SCB[o]);
@@ -184,7 +230,7 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gemv_i8_kernel<T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  gemv_i8_kernel<T><<<kSmCount, kGvThreads, smem, s>>>(
+  gemv_i8_kernel<T><<<kSmCount, GvShape<T>::kThreads, smem, s>>>(
       a.CB, a.SCB, a.in, a.out, a.xq8, a.rowabs, a.hdr, a.idx,
       static_cast<const uint16_t*>(a.xout), a.ncap, static_cast<const uint16_t*>(a.bias),
       static_cast<uint16_t*>(a.Y), a.acc_debug, use_tab ? 1 : 0);
