@@ -7,11 +7,15 @@ CUDA package: the two sides only share the seeded input generators in ``synth``.
 The arithmetic lives in ``int8mm_oracle.c`` (plain C, IEEE fp32 for the quantizers, exact
 integers for the int8 products, fp64 for the output). This module is numpy marshalling.
 
+The FFN block (``ffn``) chains two of these matmuls with ReLU (or nothing) between them,
+the intermediate rounded once from fp64 to fp16 as the second matmul's input.
+
 Pins (checked by ``tests/test_oracle.py`` without a GPU): the pages' worked absmax example,
 an integer-valued case where the method reduces to an exact integer matmul, the
 quantization error bounds, threshold = inf reducing to plain vector-wise int8, zeroing the
 outlier columns reproducing the inlier product, the zeropoint range and round-trip
-bounds, and brute-force outlier sets on tiny inputs. The quality of the method against
+bounds, brute-force outlier sets on tiny inputs, and integer-valued FFN blocks (with and
+without outlier columns in either matmul) that reduce to exact integer matmuls with ReLU. The quality of the method against
 the unquantized product is reported, not pinned (the pages print no per-matmul error).
 """
 from __future__ import annotations
@@ -42,6 +46,7 @@ def load(path: str) -> C.CDLL:
     L.orc_int8_matmul.restype = C.c_int32
     L.orc_half_to_float.argtypes = [p, i64, p]
     L.orc_float_to_half.argtypes = [p, i64, p]
+    L.orc_activation_to_half.argtypes = [p, i64, C.c_int, p]
     return L
 
 
@@ -165,3 +170,30 @@ def int8_matmul(X, CB, SCB, threshold=6.0, bias=None, rows=None, nthreads=None,
                               _ptr(rows), nr, _ptr(Y), _ptr(acc), _ptr(Q), _ptr(ra), _ptr(idx),
                               int(nthreads or default_threads()))
     return {"Y": Y, "acc": acc, "Q": Q, "rowabs": ra, "idx": idx[:n].copy(), "rows": rows}
+
+
+def activation_to_half(y: np.ndarray, relu: bool) -> np.ndarray:
+    """fp16(act(y)) for fp64 y: ReLU (y <= 0 -> +0) or identity, one rounding to nearest."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    h = np.empty(y.shape, np.uint16)
+    lib().orc_activation_to_half(_ptr(y), y.size, 1 if relu else 0, _ptr(h))
+    return h.view(np.float16)
+
+
+def ffn(X, CB_up, SCB_up, CB_down, SCB_down, threshold=6.0, bias_up=None, bias_down=None,
+        act="relu", nthreads=None):
+    """FFN block of two LLM.int8() matmuls: H = act(matmul(X, up)) rounded to fp16, then
+    Y = matmul(H, down), each matmul with its own outlier decomposition.
+
+    Returns a dict: H_exact (fp64 act of the first matmul's output), H (fp16, the second
+    matmul's input), Y (fp64), up_idx and down_idx (the two outlier column sets)."""
+    if act not in ("relu", "none"):
+        raise ValueError(act)
+    up = int8_matmul(X, CB_up, SCB_up, threshold, bias_up, nthreads=nthreads, want_acc=False)
+    relu = act == "relu"
+    H_exact = np.maximum(up["Y"], 0.0) if relu else up["Y"]
+    H = activation_to_half(up["Y"], relu)
+    down = int8_matmul(H, CB_down, SCB_down, threshold, bias_down, nthreads=nthreads,
+                       want_acc=False)
+    return {"H_exact": H_exact, "H": H, "Y": down["Y"], "up_idx": up["idx"],
+            "down_idx": down["idx"]}

@@ -157,6 +157,18 @@ void orc_zeropoint_rows(const uint16_t* X, int64_t rows, int64_t cols, int8_t* Q
   }
 }
 
+/* FFN block intermediate: H = fp16(act(y)) for the fp64 output y of the first matmul,
+ * act = identity (relu == 0) or ReLU (max(y, 0); y <= 0 gives +0). One rounding from
+ * fp64 to fp16, to nearest even. */
+void orc_activation_to_half(const double* y, int64_t n, int relu, uint16_t* h) {
+  for (int64_t i = 0; i < n; ++i) {
+    double v = y[i];
+    if (relu && !(v > 0.0)) v = 0.0;
+    _Float16 t = (_Float16)v;
+    memcpy(&h[i], &t, sizeof t);
+  }
+}
+
 /* ---------------------------------------------------------------- full matmul */
 
 typedef struct {

@@ -260,3 +260,57 @@ def test_zeropoint_zero_maps_exactly_and_constant_row():
     assert S[1] == 0 and Z[1] == 2.5 and not Q[1].any()
     rec = oracle.zeropoint_dequant(Q, S, Z)
     assert (rec[1] == 2.5).all()
+
+
+# --------------------------------------------------------------------------- FFN block
+@pytest.mark.parametrize("outliers", [False, True])
+def test_integer_ffn_block_reduces_to_exact_integer_chain(outliers):
+    """With weights of absmax 1 and activations whose inlier absmax is 1 (or 0), every code
+    is 127 times the value and both matmuls are exact, so the block equals the integer
+    chain relu(X W_up^T) W_down^T + b_down, computed here with numpy integer matmuls. With
+    outliers, column 0 of X (value 8) and the big features of H (values 6..10) are the two
+    outlier sets at threshold 6."""
+    d = synth.make_integer_ffn(3, 37, 64, 160, outliers)
+    thr = 6.0 if outliers else math.inf
+    CBu, SCBu = oracle.quantize_weight(d["W_up"])
+    CBd, SCBd = oracle.quantize_weight(d["W_down"])
+    r = oracle.ffn(d["X"], CBu, SCBu, CBd, SCBd, thr, None, d["b_down"], "relu", nthreads=2)
+    Xi = d["X"].astype(np.int64)
+    pre = Xi @ d["W_up"].astype(np.int64).T
+    assert pre.min() < 0                       # the ReLU has work to do
+    Hi = np.maximum(pre, 0)
+    Yi = Hi @ d["W_down"].astype(np.int64).T + d["b_down"].astype(np.int64)
+    assert np.array_equal(r["H_exact"], Hi.astype(np.float64))
+    assert np.array_equal(r["H"].astype(np.int64), Hi)
+    assert np.array_equal(r["Y"], Yi.astype(np.float64))
+    if outliers:
+        assert r["up_idx"].tolist() == [0]
+        assert r["down_idx"].tolist() == d["big"].tolist()
+        assert (Hi[:, d["big"]] >= 6).all()
+    else:
+        assert r["up_idx"].size == 0 and r["down_idx"].size == 0
+
+
+def test_ffn_without_activation_is_two_chained_matmuls():
+    """act = none: H is the first matmul's output rounded to fp16 (negative values kept)."""
+    d = synth.make_integer_ffn(4, 9, 32, 64, True)
+    CBu, SCBu = oracle.quantize_weight(d["W_up"])
+    CBd, SCBd = oracle.quantize_weight(d["W_down"])
+    r = oracle.ffn(d["X"], CBu, SCBu, CBd, SCBd, 6.0, None, d["b_down"], "none", nthreads=1)
+    pre = d["X"].astype(np.int64) @ d["W_up"].astype(np.int64).T
+    assert pre.min() < 0
+    assert np.array_equal(r["H"].astype(np.int64), pre)
+    Yi = pre @ d["W_down"].astype(np.int64).T + d["b_down"].astype(np.int64)
+    assert np.array_equal(r["Y"], Yi.astype(np.float64))
+
+
+def test_activation_rounding_is_one_step_from_fp64():
+    """fp64 -> fp16 once, ties to even, ReLU zeros (including -0 and tiny negatives) become
+    +0; values beyond the fp16 range round to infinity."""
+    y = np.array([-3.5, -1e-30, -0.0, 0.0, 2049.0, 2051.0, 2049.0 + 2.0**-30, 65519.99,
+                  65520.0, 1.0 + 2.0**-11])
+    h = oracle.activation_to_half(y, relu=True)
+    assert h.view(np.uint16).tolist()[:4] == [0, 0, 0, 0]
+    assert h[4:].tolist() == [2048.0, 2052.0, 2050.0, 65504.0, math.inf, 1.0]
+    g = oracle.activation_to_half(y, relu=False)
+    assert g[0] == -3.5 and g.view(np.uint16)[1] == 0x8000 and g[4] == 2048.0

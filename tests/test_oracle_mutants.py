@@ -23,6 +23,10 @@ MUTANTS = [
     ("scale 128 instead of 127", "? 127.0f / absmax", "? 128.0f / absmax"),
     ("outlier weight not dequantized", "* SCB[o]) / 127.0f", "* 1.0f) / 127.0f"),
     ("bias subtracted", "y += (double)h2f(jb->bias[o]);", "y -= (double)h2f(jb->bias[o]);"),
+    ("ReLU dropped", "if (relu && !(v > 0.0)) v = 0.0;", "if (relu && 0) v = 0.0;"),
+    ("ReLU mirrors negatives", "if (relu && !(v > 0.0)) v = 0.0;",
+     "if (relu && !(v > 0.0)) v = -v;"),
+    ("intermediate rounded twice", "_Float16 t = (_Float16)v;", "_Float16 t = (_Float16)(float)v;"),
 ]
 
 PIN_TESTS = [
@@ -35,6 +39,9 @@ PIN_TESTS = [
     pins.test_acc_equals_library_integer_matmul_and_codes_in_range,
     pins.test_zeropoint_uses_full_range_on_one_sided_rows,
     pins.test_zeropoint_zero_maps_exactly_and_constant_row,
+    lambda: pins.test_integer_ffn_block_reduces_to_exact_integer_chain(True),
+    pins.test_ffn_without_activation_is_two_chained_matmuls,
+    pins.test_activation_rounding_is_one_step_from_fp64,
 ]
 
 
