@@ -13,7 +13,8 @@ is bracketed by a barrier and a device synchronize, and the time is the max over
 The reference arm (`--impl reference`) is the CPU oracle on the host cores, timed on a
 bounded sample of rows of the same workload.
 
-Prints one JSON line (rank 0).
+Prints one JSON line (rank 0). `--all` prints one line per configuration, then the FFN
+block line (`--ffn` alone prints only that one) and the standalone row quantizers.
 """
 from __future__ import annotations
 
@@ -38,6 +39,9 @@ DEFAULT_WORKLOAD = "ffn_6.7b_up"
 ALL_CONFIGS = ["ffn_6.7b_up", "ffn_13b_up", "ffn_13b_down", "decode_176b_t1", "decode_176b_t8",
                "decode_176b_t64", "sweep_f0_thr6", "sweep_f0.1_thr6", "sweep_f0.5_thr6",
                "sweep_f2_thr6", "sweep_f0_thrinf", "sweep_f2_thrinf"]
+FFN_METRIC = ("int8_ffn TOPS on the FFN block (X W_up^T -> ReLU -> W_down^T, LLM.int8() "
+              "in both)")
+DEFAULT_FFN = "ffn_13b_block"
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -467,6 +471,165 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+def run_ffn(args) -> None:
+    """The FFN block (int8_ffn) on one GPU: up projection with ReLU and the down
+    projection's column flags in its epilogue, mask compaction, down projection."""
+    import torch
+    import int8_mixed_precision_03_b300 as i8
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    f = synth.FFN_WORKLOADS[args.ffn_workload]
+    blk = synth.make_ffn(f)
+    X = torch.from_numpy(blk["X"]).to(device)
+    bu, bd = (torch.from_numpy(blk[k]).to(device) for k in ("b_up", "b_down"))
+    Wu, Wd = (torch.from_numpy(blk[k]).to(device) for k in ("W_up", "W_down"))
+    CBu, SCBu = i8.int8_quantize_weight(Wu)
+    CBd, SCBd = i8.int8_quantize_weight(Wd)
+    ws = torch.empty(i8.int8_ffn_workspace_size(f.T, f.d_model, f.d_ff), dtype=torch.uint8,
+                     device=device)
+    H = torch.empty((f.T, f.d_ff), dtype=torch.float16, device=device)
+    Y = torch.empty((f.T, f.d_model), dtype=torch.float16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    thr = f.threshold
+
+    def step(x=X, h=H, y=Y, w=ws):
+        i8.int8_ffn(x, CBu, SCBu, CBd, SCBd, thr, bu, bd, "relu", H=h, Y=y, workspace=w)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if i8.i8_get_status(ws) != 0:
+        raise RuntimeError(f"device status {i8.i8_get_status(ws)} after warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in [x for row in ev for x in row] + st + en:
+        e.record()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    launches = 0
+    for k in range(K):
+        flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
+        i8.i8_set_profile_events(ev[k])
+        st[k].record()
+        step()
+        en[k].record()
+        launches += 6    # statistics, quantize, matmul of the up projection; mask
+                         # compaction, quantize, matmul of the down projection
+    i8.i8_set_profile_events(None)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    clk = clocks.stop()
+    if i8.i8_get_status(ws) != 0:
+        raise RuntimeError(f"device status {i8.i8_get_status(ws)} in the timed region")
+    step_ms = statistics.mean(st[k].elapsed_time(en[k]) for k in range(K))
+    names = ["up_colstats", "up_quantize_gather", "up_matmul", "down_mask_index",
+             "down_quantize_gather", "down_matmul"]
+    pairs = [(0, 1), (1, 2), (2, 3), (4, 5), (5, 6), (6, 7)]
+    k_ms = {n: statistics.mean(ev[k][a].elapsed_time(ev[k][b]) for k in range(K))
+            for n, (a, b) in zip(names, pairs)}
+    ops = 4.0 * f.T * f.d_model * f.d_ff
+    value = ops / (step_ms / 1e3) / 1e12
+
+    def timed(fn, n):
+        out = []
+        for k in range(n + 3):
+            flush.fill_(k & 0xff)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            if k >= 3:
+                out.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in out)
+
+    Kc = min(K, 50)
+    ws_u = i8.alloc_workspace(f.T, f.d_model, f.d_ff, device)
+    ws_d = i8.alloc_workspace(f.T, f.d_ff, f.d_model, device)
+    H2, Y2 = torch.empty_like(H), torch.empty_like(Y)
+
+    def two_calls():  # the same block without the fused statistics (torch ReLU between)
+        i8.int8_matmul(X, CBu, SCBu, thr, bu, Y=H2, workspace=ws_u)
+        torch.relu_(H2)
+        i8.int8_matmul(H2, CBd, SCBd, thr, bd, Y=Y2, workspace=ws_d)
+
+    two_ms = timed(two_calls, Kc)
+    f16_ms = timed(lambda: i8.f16_ffn(X, Wu, Wd, bu, bd, "relu", H=H2, Y=Y2), Kc)
+
+    # end to end through the public call: X in from pinned host memory, Y back, two streams
+    Xpin = torch.from_numpy(blk["X"]).pin_memory()
+    nbuf = 2
+    streams = [torch.cuda.Stream(device) for _ in range(nbuf)]
+    Xe = [torch.empty_like(X) for _ in range(nbuf)]
+    He = [torch.empty_like(H) for _ in range(nbuf)]
+    Ye = [torch.empty_like(Y) for _ in range(nbuf)]
+    Ype = [torch.empty(Y.shape, dtype=torch.float16).pin_memory() for _ in range(nbuf)]
+    wse = [ws] + [torch.empty_like(ws) for _ in range(nbuf - 1)]
+
+    def e2e_steps(n):
+        start = torch.cuda.current_stream(device)
+        for s_ in streams:
+            s_.wait_stream(start)
+        for k in range(n):
+            b = k % nbuf
+            with torch.cuda.stream(streams[b]):
+                Xe[b].copy_(Xpin, non_blocking=True)
+                step(Xe[b], He[b], Ye[b], wse[b])
+                Ype[b].copy_(Ye[b], non_blocking=True)
+        for s_ in streams:
+            start.wait_stream(s_)
+
+    e2e_steps(2 * nbuf)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    e2e_steps(Kc)
+    e1.record()
+    torch.cuda.synchronize()
+    for b in range(nbuf):
+        if i8.i8_get_status(wse[b]) != 0:
+            raise RuntimeError(f"device status {i8.i8_get_status(wse[b])} in the e2e run")
+    e2e_s = e0.elapsed_time(e1) / 1e3
+
+    peaks, peak_src = load_peaks()
+    mm_ms = k_ms["up_matmul"] + k_ms["down_matmul"]
+    achieved = ops / (mm_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": FFN_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": f.name, "T": f.T, "d_model": f.d_model, "d_ff": f.d_ff,
+                   "threshold": thr, "act": "relu",
+                   "n_outlier_cols_x": f.x_workload().n_outlier_cols,
+                   "n_outlier_features_h": f.n_h_outliers(), "parallelism": "single",
+                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+        "kernels_us": {k: round(v * 1e3, 2) for k, v in k_ms.items()},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "kernel": "i8_gemm_kernel (both projections; the up projection's "
+                               "epilogue with ReLU and the down projection's column flags)",
+                     "peak_source": f"bf16_tflops burst, {peak_src} (MEASURED_PEAKS.json)"},
+        "two_call_us": round(two_ms * 1e3, 2),
+        "fusion_speedup": two_ms / step_ms,
+        "f16_comparator": {"us": round(f16_ms * 1e3, 2),
+                           "TFLOP/s": ops / (f16_ms / 1e3) / 1e12,
+                           "frac_of_bf16_peak": ops / (f16_ms / 1e3) / 1e12 / peak,
+                           "int8_step_speedup": f16_ms / step_ms},
+        "e2e": {"value": ops * Kc / e2e_s / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(Xpin.numel() * 2),
+                "d2h_bytes_per_step": int(Ype[0].numel() * 2), "steps": Kc,
+                "overlap": "2 streams: a step's copies overlap its neighbours"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_rows(args) -> None:
     """Standalone row quantizers on the sweep's X [1024, 8192] (absmax on N(0,1) with the
     sweep's outliers, zeropoint on |N(0,1)|): HBM-bound, reported in GB/s."""
@@ -522,6 +685,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", action="store_true",
                     help="one line per configuration (1 GPU, no CPU baseline)")
+    ap.add_argument("--ffn", action="store_true", help="only the FFN block line (1 GPU)")
+    ap.add_argument("--ffn-workload", default=DEFAULT_FFN, choices=sorted(synth.FFN_WORKLOADS))
     args = ap.parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
@@ -532,7 +697,12 @@ def main(argv=None) -> None:
         for name in ALL_CONFIGS:
             args.workload = name
             run_ours(args)
+        run_ffn(args)
         run_rows(args)
+    elif args.ffn:
+        if dist_env()[1] > 1:
+            raise SystemExit("--ffn runs on one GPU")
+        run_ffn(args)
     else:
         run_ours(args)
 

@@ -89,12 +89,14 @@ size_t int8_matmul_workspace_size(int T, int in, int out, int max_outlier_cols);
  *               The outlier capacity used is the largest multiple of 64 columns that fits
  *               in ws_bytes. Contents on entry are ignored. Two calls that run at the same
  *               time must not share a workspace.
- * `in` must be a multiple of 16 and <= I8_MAX_IN; T == 0 or out == 0 is a no-op.
+ * `in` must be a multiple of 16 and <= I8_MAX_IN; T == 0 or out == 0 is a no-op (with
+ * T == 0, X and Y may be NULL).
  * Launches: one memset of the workspace header and three kernels (column statistics,
  * row quantize + outlier gather, matmul). The matmul is the tensor-core kernel, or, for
- * decode sizes (T <= 8 with T*in <= 200 KB), a CUDA-core kernel that streams CB at HBM rate
- * with exact int32 dp4a sums. The outlier count stays on the device; no host
- * synchronization.
+ * decode sizes, a kernel that streams CB at HBM rate: T <= 8 with T*in <= 200 KB on the
+ * CUDA cores (exact int32 dp4a sums), 9 <= T <= 16 with the padded codes in 200 KB on
+ * mma.sync (exact fp32 fragments drained to int32). The outlier count stays on the device;
+ * no host synchronization.
  */
 i8_status int8_matmul(const void* X, int T, int in, const int8_t* CB, const float* SCB, int out,
                       float threshold, const void* bias, void* Y, void* workspace,
@@ -141,6 +143,68 @@ i8_status zeropoint_quantize_rows(const void* X, int rows, int cols, int8_t* Q, 
  */
 i8_status f16_matmul(const void* X, int T, int in, const void* W, int out, const void* bias,
                      void* Y, void* stream);
+
+/* Activation between the two matmuls of int8_ffn / f16_ffn. */
+#define I8_ACT_NONE 0
+#define I8_ACT_RELU 1
+
+/*
+ * Bytes of device workspace int8_ffn needs: the workspaces of its two matmuls (each with
+ * an outlier capacity of max_outlier_cols rounded up to 64, at most its own input width;
+ * <= 0 means the input width). Returns 0 for invalid sizes.
+ */
+size_t int8_ffn_workspace_size(int T, int d_model, int d_ff, int max_outlier_cols);
+
+/*
+ * An FFN block of two LLM.int8() matmuls, H = act(X . W_up^T + b_up) and
+ * Y = H . W_down^T + b_down, each with the decomposition of int8_matmul ("LLM.int8()
+ * summary" (zenn), section "INT8 speed": the benchmarked matmul is an FFN layer whose
+ * intermediate size is four times the model size).
+ *   X                  : fp16 [T, d_model]
+ *   CB_up, SCB_up      : int8_quantize_weight of W_up [d_ff, d_model]
+ *   CB_down, SCB_down  : int8_quantize_weight of W_down [d_model, d_ff]
+ *   bias_up, bias_down : fp16 [d_ff], [d_model] or NULL
+ *   threshold          : outlier threshold of both matmuls (as in int8_matmul)
+ *   act                : I8_ACT_NONE or I8_ACT_RELU (H = max(y, 0)); else I8_ERR_INVALID_ARG
+ *   H                  : fp16 [T, d_ff]    output: the intermediate activations
+ *   Y                  : fp16 [T, d_model] output
+ *   workspace          : ws_bytes >= int8_ffn_workspace_size(...); the capacity used is the
+ *                        largest multiple of 64 columns that fits for both matmuls
+ * H and Y are exactly what int8_matmul(X, up) -> act -> int8_matmul(H, down) gives; the
+ * difference is where step 1 of the second matmul happens: the first matmul's epilogue
+ * applies `act` and ORs each column of H whose fp16 magnitude reaches the threshold into
+ * the second matmul's outlier mask, so H is not read an extra time for its column
+ * statistics. d_model and d_ff must be multiples of 16 (<= I8_MAX_IN); T == 0 is a no-op
+ * (X, H and Y may then be NULL).
+ * Launches: two memsets and six kernels. Device errors of either matmul (outlier capacity,
+ * timeout) end up in the one status word i8_get_status(workspace) reads, the first one
+ * in stream order. With act == I8_ACT_NONE the second matmul's statistics are taken the
+ * same way.
+ */
+i8_status int8_ffn(const void* X, int T, int d_model, int d_ff, const int8_t* CB_up,
+                   const float* SCB_up, const void* bias_up, const int8_t* CB_down,
+                   const float* SCB_down, const void* bias_down, float threshold, int act,
+                   void* H, void* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * int8_ffn plus the second matmul's outlier columns, for tests (either pointer may be
+ * NULL): down_outlier_idx int32 [d_ff] (first *down_n_out valid, ascending),
+ * down_n_out int32 [1].
+ */
+i8_status int8_ffn_debug(const void* X, int T, int d_model, int d_ff, const int8_t* CB_up,
+                         const float* SCB_up, const void* bias_up, const int8_t* CB_down,
+                         const float* SCB_down, const void* bias_down, float threshold,
+                         int act, void* H, void* Y, void* workspace, size_t ws_bytes,
+                         void* stream, int32_t* down_outlier_idx, int32_t* down_n_out);
+
+/*
+ * The fp16 comparator of int8_ffn: f16_matmul(X, W_up) with `act` in its epilogue, then
+ * f16_matmul(H, W_down). W_up fp16 [d_ff, d_model], W_down fp16 [d_model, d_ff]; H, Y as
+ * in int8_ffn. Two kernel launches.
+ */
+i8_status f16_ffn(const void* X, int T, int d_model, int d_ff, const void* W_up,
+                  const void* bias_up, const void* W_down, const void* bias_down, int act,
+                  void* H, void* Y, void* stream);
 
 /*
  * Synchronizes `stream` and returns the device status word of the last int8_matmul that
@@ -202,10 +266,18 @@ i8_status int8_matmul_noalloc(const void* X, int T, int in, const int8_t* CB, co
  * Profiling aid. `events` is NULL (off) or an array of 4 cudaEvent_t handles owned by the
  * caller. While set, every int8_matmul / int8_matmul_debug on this host thread records
  * events[0] before the column statistics, events[1] before the quantize pass, events[2]
- * before the tensor-core matmul and events[3] after it, on the call's stream, so that the
+ * before the matmul kernel and events[3] after it, on the call's stream, so that the
  * caller can time each kernel with cudaEventElapsedTime. Changes nothing else.
  */
 void i8_set_profile_events(void** events);
+
+/*
+ * The same with n events (at most 8; NULL or n <= 0: off). int8_matmul records events
+ * 0..3 as above; int8_ffn / int8_ffn_debug record 0..3 around its first matmul and 4..7
+ * around its second (events[4] before the mask compaction that replaces its column
+ * statistics). Slots beyond n are not recorded.
+ */
+void i8_set_profile_events_n(void** events, int n);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libint8mm.so")
 
 I8_OK = 0
+ACT = {"none": 0, "relu": 1}  # I8_ACT_NONE, I8_ACT_RELU
 STATUS = {0: "I8_OK", 1: "I8_ERR_INVALID_ARG", 2: "I8_ERR_ALIGNMENT", 3: "I8_ERR_WORKSPACE",
           4: "I8_ERR_UNSUPPORTED_DEVICE", 5: "I8_ERR_CUDA", 6: "I8_ERR_OUTLIER_CAP",
           7: "I8_ERR_TIMEOUT", 8: "I8_ERR_SCRATCH_LIMIT"}
@@ -32,11 +33,17 @@ SIGNATURES = {
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
     "zeropoint_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p, _p]),
     "f16_matmul": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
+    "int8_ffn_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "int8_ffn": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _f, _i, _p, _p, _p, _sz, _p]),
+    "int8_ffn_debug": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _f, _i, _p, _p, _p, _sz,
+                            _p, _p, _p]),
+    "f16_ffn": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _i, _p, _p, _p]),
     "i8_test_stalled_matmul": (_i, [_p, _i, _i, _p, _p, _i, _p, _p, _sz, C.c_uint64, _p]),
     "i8_get_status": (_i, [_p, _p]),
     "i8_status_string": (C.c_char_p, [_i]),
     "i8_last_launch_count": (_i, []),
     "i8_set_profile_events": (None, [_p]),
+    "i8_set_profile_events_n": (None, [_p, _i]),
 }
 
 _lib = None
@@ -208,6 +215,90 @@ def f16_matmul(X: torch.Tensor, W: torch.Tensor, bias: torch.Tensor | None = Non
     return Y
 
 
+def int8_ffn_workspace_size(T: int, d_model: int, d_ff: int, max_outlier_cols: int = 0) -> int:
+    return int(lib().int8_ffn_workspace_size(T, d_model, d_ff, max_outlier_cols))
+
+
+def _act(act: str) -> int:
+    if act not in ACT:
+        raise ValueError(f"act must be one of {sorted(ACT)}")
+    return ACT[act]
+
+
+def _ffn_args(X, CB_up, SCB_up, CB_down, SCB_down, bias_up, bias_down, H, Y, workspace):
+    _need(X, torch.float16, "X")
+    for t, dt, name in ((CB_up, torch.int8, "CB_up"), (SCB_up, torch.float32, "SCB_up"),
+                        (CB_down, torch.int8, "CB_down"), (SCB_down, torch.float32, "SCB_down")):
+        _need(t, dt, name)
+    for t, name in ((bias_up, "bias_up"), (bias_down, "bias_down")):
+        if t is not None:
+            _need(t, torch.float16, name)
+    T, d = X.shape
+    d_ff = CB_up.shape[0]
+    if CB_up.shape[1] != d or tuple(CB_down.shape) != (d, d_ff):
+        raise ValueError("CB_up must be [d_ff, d_model] and CB_down [d_model, d_ff]")
+    dev = X.device
+    if H is None:
+        H = torch.empty((T, d_ff), dtype=torch.float16, device=dev)
+    if Y is None:
+        Y = torch.empty((T, d), dtype=torch.float16, device=dev)
+    if workspace is None:
+        n = int8_ffn_workspace_size(T, d, d_ff)
+        if n == 0:
+            raise ValueError("invalid sizes for int8_ffn")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    return T, d, d_ff, H, Y, workspace
+
+
+def int8_ffn(X, CB_up, SCB_up, CB_down, SCB_down, threshold: float = 6.0, bias_up=None,
+             bias_down=None, act: str = "relu", H=None, Y=None, workspace=None):
+    """FFN block of two LLM.int8() matmuls: H = act(X W_up^T + b_up), Y = H W_down^T + b_down,
+    with the second matmul's column statistics taken in the first one's epilogue.
+    Returns (H, Y)."""
+    T, d, d_ff, H, Y, workspace = _ffn_args(X, CB_up, SCB_up, CB_down, SCB_down, bias_up,
+                                            bias_down, H, Y, workspace)
+    _check("int8_ffn", lib().int8_ffn(
+        _ptr(X), T, d, d_ff, _ptr(CB_up), _ptr(SCB_up), _ptr(bias_up), _ptr(CB_down),
+        _ptr(SCB_down), _ptr(bias_down), float(threshold), _act(act), _ptr(H), _ptr(Y),
+        _ptr(workspace), workspace.numel(), _stream(X.device)))
+    return H, Y
+
+
+def int8_ffn_debug(X, CB_up, SCB_up, CB_down, SCB_down, threshold: float = 6.0, bias_up=None,
+                   bias_down=None, act: str = "relu", workspace=None):
+    """int8_ffn plus the second matmul's outlier columns: dict of H, Y, down_idx, down_n_out
+    and the workspace."""
+    T, d, d_ff, H, Y, workspace = _ffn_args(X, CB_up, SCB_up, CB_down, SCB_down, bias_up,
+                                            bias_down, None, None, workspace)
+    dev = X.device
+    idx = torch.full((d_ff,), -1, dtype=torch.int32, device=dev)
+    n = torch.zeros(4, dtype=torch.int32, device=dev)
+    _check("int8_ffn_debug", lib().int8_ffn_debug(
+        _ptr(X), T, d, d_ff, _ptr(CB_up), _ptr(SCB_up), _ptr(bias_up), _ptr(CB_down),
+        _ptr(SCB_down), _ptr(bias_down), float(threshold), _act(act), _ptr(H), _ptr(Y),
+        _ptr(workspace), workspace.numel(), _stream(dev), _ptr(idx), _ptr(n)))
+    n_out = int(n[0].item()) if T > 0 else 0
+    return {"H": H, "Y": Y, "down_idx": idx[:n_out], "down_n_out": n_out,
+            "workspace": workspace}
+
+
+def f16_ffn(X, W_up, W_down, bias_up=None, bias_down=None, act: str = "relu", H=None, Y=None):
+    """The fp16 comparator of int8_ffn on our tcgen05 fp16 GEMM. Returns (H, Y)."""
+    _need(X, torch.float16, "X")
+    _need(W_up, torch.float16, "W_up")
+    _need(W_down, torch.float16, "W_down")
+    T, d = X.shape
+    d_ff = W_up.shape[0]
+    if H is None:
+        H = torch.empty((T, d_ff), dtype=torch.float16, device=X.device)
+    if Y is None:
+        Y = torch.empty((T, d), dtype=torch.float16, device=X.device)
+    _check("f16_ffn", lib().f16_ffn(_ptr(X), T, d, d_ff, _ptr(W_up), _ptr(bias_up),
+                                    _ptr(W_down), _ptr(bias_down), _act(act), _ptr(H), _ptr(Y),
+                                    _stream(X.device)))
+    return H, Y
+
+
 def i8_get_status(workspace: torch.Tensor) -> int:
     """Synchronizes the current stream and returns the workspace's device status code."""
     return int(lib().i8_get_status(_ptr(workspace), _stream(workspace.device)))
@@ -218,13 +309,14 @@ def i8_last_launch_count() -> int:
 
 
 def i8_set_profile_events(events) -> None:
-    """events: None, or 4 torch.cuda.Event(enable_timing=True) recorded around the three
-    kernels of every following int8_matmul on this thread."""
+    """events: None, or 4 (int8_matmul) or 8 (int8_ffn: both matmuls)
+    torch.cuda.Event(enable_timing=True), recorded around the kernels of every following
+    call on this thread."""
     if events is None:
-        lib().i8_set_profile_events(None)
+        lib().i8_set_profile_events_n(None, 0)
         return
     for e in events:  # torch creates the CUDA event on its first record
         if e.cuda_event == 0:
             e.record()
-    arr = (C.c_void_p * 4)(*[C.c_void_p(e.cuda_event) for e in events])
-    lib().i8_set_profile_events(C.cast(arr, C.c_void_p))
+    arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
+    lib().i8_set_profile_events_n(C.cast(arr, C.c_void_p), len(events))

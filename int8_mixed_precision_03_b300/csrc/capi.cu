@@ -1,5 +1,6 @@
 // C-ABI entry points of libint8mm (declared in include/int8mm.h): host-side validation,
 // workspace layout and the launch sequence. Nothing here computes on the host.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -11,10 +12,12 @@ namespace i8mm {
 namespace {
 
 thread_local int g_last_launches = 0;
-thread_local cudaEvent_t g_prof[4] = {nullptr, nullptr, nullptr, nullptr};
+constexpr int kProfSlots = 8;
+thread_local cudaEvent_t g_prof[kProfSlots] = {};
+thread_local int g_prof_n = 0;
 
 void prof_mark(int i, cudaStream_t s) {
-  if (g_prof[i]) cudaEventRecord(g_prof[i], s);
+  if (i >= 0 && i < g_prof_n && g_prof[i]) cudaEventRecord(g_prof[i], s);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -60,11 +63,120 @@ i8_status validate_matmul(const void* X, int T, int in, const int8_t* CB, const 
                           const void* ws) {
   if (T < 0 || out < 0 || in <= 0 || in > I8_MAX_IN) return I8_ERR_INVALID_ARG;
   if (std::isnan(threshold) || threshold <= 0.0f) return I8_ERR_INVALID_ARG;
-  if (!X || !CB || !SCB || !Y || !ws) return I8_ERR_INVALID_ARG;
+  if (!CB || !SCB || !ws) return I8_ERR_INVALID_ARG;
+  if (T > 0 && (!X || !Y)) return I8_ERR_INVALID_ARG;  // an empty batch may pass nulls
   if (in % 16 != 0) return I8_ERR_ALIGNMENT;
   if (!aligned16(X) || !aligned16(CB) || !aligned16(SCB) || !aligned16(Y) || !aligned16(ws) ||
       (bias && !aligned16(bias)))
     return I8_ERR_ALIGNMENT;
+  return I8_OK;
+}
+
+// One int8 matmul on its (already zeroed) workspace section: column statistics (or, when
+// the previous matmul's epilogue has filled the mask, only its compaction), quantize +
+// gather, then the tensor-core or decode matmul with the optional epilogue extras.
+struct Layer {
+  const void* X = nullptr;
+  int T = 0, in = 0, out = 0;
+  const int8_t* CB = nullptr;
+  const float* SCB = nullptr;
+  uint16_t thr_bits = 0x7C00u;
+  const void* bias = nullptr;
+  void* Y = nullptr;
+  uint8_t* ws = nullptr;
+  WsLayout L;
+  NextLayer next;                  // FFN up projection: activation + next layer's mask
+  bool stats_in_mask = false;      // the mask was filled by the previous matmul
+  const WsHeader* prev = nullptr;  // its status word, carried into this one
+  int8_t* dbg_xq = nullptr;
+  int32_t* dbg_acc = nullptr;
+  uint64_t stall_ns = 0;
+  int prof_base = -1;              // profiling events prof_base .. +3, or -1: none
+};
+
+i8_status launch_layer(const Layer& ly, cudaStream_t s) {
+  const WsLayout& L = ly.L;
+  uint8_t* ws = ly.ws;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(ws + L.mask);
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
+  float* rowabs = reinterpret_cast<float*>(ws + L.rowabs);
+  int32_t* l1 = reinterpret_cast<int32_t*>(ws + L.l1);
+  const int ncap = L.ncap;
+  i8_status st;
+  if (ly.prof_base >= 0) prof_mark(ly.prof_base + 0, s);
+  if (ly.stats_in_mask)
+    st = from_cuda(launch_mask_index(ly.in, hdr, mask, idx, ncap, ly.prev, s));
+  else
+    st = from_cuda(launch_colstats(ly.X, ly.T, ly.in, ly.thr_bits, hdr, mask, idx, ncap, s));
+  if (st != I8_OK) return st;
+  ++g_last_launches;
+  if (ly.prof_base >= 0) prof_mark(ly.prof_base + 1, s);
+  if (gemv_fits(ly.T, ly.in)) {
+    // decode sizes: int8 codes for the CUDA-core matmul, which reads the outlier weights
+    // from CB itself (no W_out gather)
+    int8_t* xq8 = reinterpret_cast<int8_t*>(ws + L.xq);
+    if ((st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
+                                               mask, idx, ncap, nullptr, rowabs, ws + L.xout,
+                                               nullptr, l1, xq8, s))) != I8_OK)
+      return st;
+    ++g_last_launches;
+    if (ly.prof_base >= 0) prof_mark(ly.prof_base + 2, s);
+    GemvArgs g;
+    g.CB = ly.CB;
+    g.SCB = ly.SCB;
+    g.T = ly.T;
+    g.in = ly.in;
+    g.out = ly.out;
+    g.xq8 = xq8;
+    g.rowabs = rowabs;
+    g.hdr = hdr;
+    g.idx = idx;
+    g.xout = ws + L.xout;
+    g.ncap = ncap;
+    g.bias = ly.bias;
+    g.Y = ly.Y;
+    g.acc_debug = ly.dbg_acc;
+    g.next = ly.next;
+    if ((st = from_cuda(launch_gemv_i8(g, s))) != I8_OK) return st;
+    ++g_last_launches;
+    if (ly.prof_base >= 0) prof_mark(ly.prof_base + 3, s);
+    if (ly.dbg_xq && cudaMemcpyAsync(ly.dbg_xq, xq8, (size_t)ly.T * ly.in,
+                                     cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return I8_ERR_CUDA;
+  } else {
+    if ((st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
+                                               mask, idx, ncap, ws + L.xq, rowabs, ws + L.xout,
+                                               ws + L.wout, l1, ly.dbg_xq, s))) != I8_OK)
+      return st;
+    ++g_last_launches;
+    if (ly.prof_base >= 0) prof_mark(ly.prof_base + 2, s);
+    GemmArgs g;
+    g.a_int8 = ly.CB;
+    g.b_f16 = ws + L.xq;
+    g.wout = ws + L.wout;
+    g.xout = ws + L.xout;
+    g.ncap = ncap;
+    g.hdr = hdr;
+    g.rowabs = rowabs;
+    g.l1 = l1;
+    g.acc_scratch = reinterpret_cast<int32_t*>(ws + L.acc);
+    g.scb = ly.SCB;
+    g.bias = ly.bias;
+    g.Y = ly.Y;
+    g.acc_debug = ly.dbg_acc;
+    g.T = ly.T;
+    g.in = ly.in;
+    g.out = ly.out;
+    g.next = ly.next;
+    if (ly.stall_ns) {  // test hook: nothing is loaded, so every pipeline wait runs out
+      g.debug_skip_loads = 1;
+      g.timeout_ns = ly.stall_ns;
+    }
+    if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
+    ++g_last_launches;
+    if (ly.prof_base >= 0) prof_mark(ly.prof_base + 3, s);
+  }
   return I8_OK;
 }
 
@@ -85,95 +197,143 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   const int ncap = ncap_for_bytes(T, in, out, ws_bytes);
   if (ncap < 64) return I8_ERR_WORKSPACE;
   if ((st = check_device()) != I8_OK) return st;
-  const WsLayout L = ws_layout(T, in, out, ncap);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
-  uint32_t* mask = reinterpret_cast<uint32_t*>(ws + L.mask);
-  int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
-  float* rowabs = reinterpret_cast<float*>(ws + L.rowabs);
-  int32_t* l1 = reinterpret_cast<int32_t*>(ws + L.l1);
-
-  if (cudaMemsetAsync(ws, 0, L.zero_bytes, s) != cudaSuccess) return I8_ERR_CUDA;
+  Layer ly;
+  ly.X = X;
+  ly.T = T;
+  ly.in = in;
+  ly.out = out;
+  ly.CB = CB;
+  ly.SCB = SCB;
+  ly.thr_bits = threshold_to_half_bits(threshold);
+  ly.bias = bias;
+  ly.Y = Y;
+  ly.ws = static_cast<uint8_t*>(workspace);
+  ly.L = ws_layout(T, in, out, ncap);
+  ly.dbg_xq = dbg_xq;
+  ly.dbg_acc = dbg_acc;
+  ly.stall_ns = stall_ns;
+  ly.prof_base = 0;
+  if (cudaMemsetAsync(ly.ws, 0, ly.L.zero_bytes, s) != cudaSuccess) return I8_ERR_CUDA;
   ++g_last_launches;
-  prof_mark(0, s);
-  if ((st = from_cuda(launch_colstats(X, T, in, threshold_to_half_bits(threshold), hdr, mask,
-                                      idx, ncap, s))) != I8_OK)
-    return st;
-  ++g_last_launches;
-  prof_mark(1, s);
-  if (gemv_fits(T, in)) {
-    // decode sizes: int8 codes for the CUDA-core matmul, which reads the outlier weights
-    // from CB itself (no W_out gather)
-    int8_t* xq8 = reinterpret_cast<int8_t*>(ws + L.xq);
-    if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
-                                               nullptr, rowabs, ws + L.xout, nullptr, l1, xq8,
-                                               s))) != I8_OK)
-      return st;
-    ++g_last_launches;
-    prof_mark(2, s);
-    GemvArgs g;
-    g.CB = CB;
-    g.SCB = SCB;
-    g.T = T;
-    g.in = in;
-    g.out = out;
-    g.xq8 = xq8;
-    g.rowabs = rowabs;
-    g.hdr = hdr;
-    g.idx = idx;
-    g.xout = ws + L.xout;
-    g.ncap = ncap;
-    g.bias = bias;
-    g.Y = Y;
-    g.acc_debug = dbg_acc;
-    if ((st = from_cuda(launch_gemv_i8(g, s))) != I8_OK) return st;
-    ++g_last_launches;
-    prof_mark(3, s);
-    if (dbg_xq && cudaMemcpyAsync(dbg_xq, xq8, (size_t)T * in, cudaMemcpyDeviceToDevice, s) !=
-                      cudaSuccess)
-      return I8_ERR_CUDA;
-  } else {
-    if ((st = from_cuda(launch_quantize_gather(X, T, in, CB, SCB, out, hdr, mask, idx, ncap,
-                                               ws + L.xq, rowabs, ws + L.xout, ws + L.wout,
-                                               l1, dbg_xq, s))) != I8_OK)
-      return st;
-    ++g_last_launches;
-    prof_mark(2, s);
-    GemmArgs g;
-    g.a_int8 = CB;
-    g.b_f16 = ws + L.xq;
-    g.wout = ws + L.wout;
-    g.xout = ws + L.xout;
-    g.ncap = ncap;
-    g.hdr = hdr;
-    g.rowabs = rowabs;
-    g.l1 = l1;
-    g.acc_scratch = reinterpret_cast<int32_t*>(ws + L.acc);
-    g.scb = SCB;
-    g.bias = bias;
-    g.Y = Y;
-    g.acc_debug = dbg_acc;
-    g.T = T;
-    g.in = in;
-    g.out = out;
-    if (stall_ns) {  // test hook: nothing is loaded, so every pipeline wait runs out
-      g.debug_skip_loads = 1;
-      g.timeout_ns = stall_ns;
-    }
-    if ((st = from_cuda(launch_i8_gemm(g, s))) != I8_OK) return st;
-    ++g_last_launches;
-    prof_mark(3, s);
-  }
+  if ((st = launch_layer(ly, s)) != I8_OK) return st;
   // debug copies of the intermediates (stream-ordered device copies)
-  if (dbg_idx && cudaMemcpyAsync(dbg_idx, idx, sizeof(int32_t) * (size_t)in,
+  uint8_t* ws = ly.ws;
+  if (dbg_idx && cudaMemcpyAsync(dbg_idx, ws + ly.L.idx, sizeof(int32_t) * (size_t)in,
                                  cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return I8_ERR_CUDA;
-  if (dbg_n && cudaMemcpyAsync(dbg_n, &hdr->n_out, sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                               s) != cudaSuccess)
+  if (dbg_n && cudaMemcpyAsync(dbg_n, &reinterpret_cast<WsHeader*>(ws + ly.L.header)->n_out,
+                               sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return I8_ERR_CUDA;
-  if (dbg_rowabs && cudaMemcpyAsync(dbg_rowabs, rowabs, sizeof(float) * (size_t)T,
+  if (dbg_rowabs && cudaMemcpyAsync(dbg_rowabs, ws + ly.L.rowabs, sizeof(float) * (size_t)T,
                                     cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return I8_ERR_CUDA;
+  return I8_OK;
+}
+
+// ---------------------------------------------------------------- FFN block
+// Workspace: [second matmul's section | first matmul's section], both 256-byte aligned, so
+// that the status word at offset 0 is the second matmul's, into which the first one's is
+// carried (launch_mask_index) before the second matmul's own kernels run.
+struct FfnPlan {
+  WsLayout down, up;
+  size_t up_off = 0, total = 0;
+};
+
+FfnPlan ffn_plan(int T, int d_model, int d_ff, int cap) {
+  FfnPlan P;
+  const int cap_up = std::min(cap, ncap_limit(d_model));
+  const int cap_down = std::min(cap, ncap_limit(d_ff));
+  P.down = ws_layout(T, d_ff, d_model, cap_down);
+  P.up = ws_layout(T, d_model, d_ff, cap_up);
+  P.up_off = align_up(P.down.total, 256);
+  P.total = P.up_off + P.up.total;
+  return P;
+}
+
+// Largest capacity (multiple of 64, at most the wider input's limit) whose plan fits.
+int ffn_cap_for_bytes(int T, int d_model, int d_ff, size_t ws_bytes) {
+  int hi = std::max(ncap_limit(d_model), ncap_limit(d_ff)) / 64, lo = 0;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (ffn_plan(T, d_model, d_ff, 64 * mid).total <= ws_bytes) lo = mid; else hi = mid - 1;
+  }
+  return 64 * lo;
+}
+
+i8_status run_ffn(const void* X, int T, int d_model, int d_ff, const int8_t* CB_up,
+                  const float* SCB_up, const void* bias_up, const int8_t* CB_down,
+                  const float* SCB_down, const void* bias_down, float threshold, int act,
+                  void* H, void* Y, void* workspace, size_t ws_bytes, void* stream,
+                  int32_t* dbg_idx, int32_t* dbg_n) {
+  g_last_launches = 0;
+  if (act != I8_ACT_NONE && act != I8_ACT_RELU) return I8_ERR_INVALID_ARG;
+  if (d_ff <= 0 || d_ff > I8_MAX_IN || !CB_down || !SCB_down) return I8_ERR_INVALID_ARG;
+  i8_status st = validate_matmul(X, T, d_model, CB_up, SCB_up, d_ff, threshold, bias_up, H,
+                                 workspace);
+  if (st != I8_OK) return st;
+  if (T > 0 && !Y) return I8_ERR_INVALID_ARG;
+  if (d_ff % 16 != 0) return I8_ERR_ALIGNMENT;
+  if (!aligned16(CB_down) || !aligned16(SCB_down) || !aligned16(Y) ||
+      (bias_down && !aligned16(bias_down)) || (dbg_idx && !aligned16(dbg_idx)) ||
+      (dbg_n && !aligned16(dbg_n)))
+    return I8_ERR_ALIGNMENT;
+  if (T == 0) return I8_OK;
+  const int cap = ffn_cap_for_bytes(T, d_model, d_ff, ws_bytes);
+  if (cap < 64) return I8_ERR_WORKSPACE;
+  if ((st = check_device()) != I8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const FfnPlan P = ffn_plan(T, d_model, d_ff, cap);
+  uint8_t* ws_down = static_cast<uint8_t*>(workspace);
+  uint8_t* ws_up = ws_down + P.up_off;
+  const uint16_t thr_bits = threshold_to_half_bits(threshold);
+
+  Layer up;
+  up.X = X;
+  up.T = T;
+  up.in = d_model;
+  up.out = d_ff;
+  up.CB = CB_up;
+  up.SCB = SCB_up;
+  up.thr_bits = thr_bits;
+  up.bias = bias_up;
+  up.Y = H;
+  up.ws = ws_up;
+  up.L = P.up;
+  up.next.relu = act == I8_ACT_RELU ? 1 : 0;
+  up.next.mask = reinterpret_cast<uint32_t*>(ws_down + P.down.mask);
+  up.next.thr_bits = thr_bits;
+
+  Layer down;
+  down.X = H;
+  down.T = T;
+  down.in = d_ff;
+  down.out = d_model;
+  down.CB = CB_down;
+  down.SCB = SCB_down;
+  down.thr_bits = thr_bits;
+  down.bias = bias_down;
+  down.Y = Y;
+  down.ws = ws_down;
+  down.L = P.down;
+  down.stats_in_mask = true;
+  down.prev = reinterpret_cast<const WsHeader*>(ws_up + P.up.header);
+  up.prof_base = 0;
+  down.prof_base = 4;
+
+  // both masks start empty: the first matmul's epilogue writes the second one's
+  if (cudaMemsetAsync(ws_down, 0, P.down.zero_bytes, s) != cudaSuccess ||
+      cudaMemsetAsync(ws_up, 0, P.up.zero_bytes, s) != cudaSuccess)
+    return I8_ERR_CUDA;
+  g_last_launches += 2;
+  if ((st = launch_layer(up, s)) != I8_OK) return st;
+  if ((st = launch_layer(down, s)) != I8_OK) return st;
+  if (dbg_idx && cudaMemcpyAsync(dbg_idx, ws_down + P.down.idx, sizeof(int32_t) * (size_t)d_ff,
+                                 cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return I8_ERR_CUDA;
+  if (dbg_n &&
+      cudaMemcpyAsync(dbg_n, &reinterpret_cast<WsHeader*>(ws_down + P.down.header)->n_out,
+                      sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return I8_ERR_CUDA;
   return I8_OK;
 }
@@ -227,6 +387,33 @@ I8_API i8_status i8_test_stalled_matmul(const void* X, int T, int in, const int8
                     nullptr, nullptr, nullptr, nullptr, nullptr, wait_limit_ns);
 }
 
+I8_API size_t int8_ffn_workspace_size(int T, int d_model, int d_ff, int max_outlier_cols) {
+  if (T < 0 || d_model <= 0 || d_ff <= 0 || d_model > I8_MAX_IN || d_ff > I8_MAX_IN) return 0;
+  const int wide = std::max(d_model, d_ff);
+  int cap = (max_outlier_cols <= 0 || max_outlier_cols > wide) ? wide : max_outlier_cols;
+  return ffn_plan(T, d_model, d_ff, (int)align_up((size_t)cap, 64)).total;
+}
+
+I8_API i8_status int8_ffn(const void* X, int T, int d_model, int d_ff, const int8_t* CB_up,
+                          const float* SCB_up, const void* bias_up, const int8_t* CB_down,
+                          const float* SCB_down, const void* bias_down, float threshold,
+                          int act, void* H, void* Y, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  return run_ffn(X, T, d_model, d_ff, CB_up, SCB_up, bias_up, CB_down, SCB_down, bias_down,
+                 threshold, act, H, Y, workspace, ws_bytes, stream, nullptr, nullptr);
+}
+
+I8_API i8_status int8_ffn_debug(const void* X, int T, int d_model, int d_ff,
+                                const int8_t* CB_up, const float* SCB_up, const void* bias_up,
+                                const int8_t* CB_down, const float* SCB_down,
+                                const void* bias_down, float threshold, int act, void* H,
+                                void* Y, void* workspace, size_t ws_bytes, void* stream,
+                                int32_t* down_outlier_idx, int32_t* down_n_out) {
+  return run_ffn(X, T, d_model, d_ff, CB_up, SCB_up, bias_up, CB_down, SCB_down, bias_down,
+                 threshold, act, H, Y, workspace, ws_bytes, stream, down_outlier_idx,
+                 down_n_out);
+}
+
 I8_API i8_status absmax_quantize_rows(const void* X, int rows, int cols, int8_t* Q,
                                       float* absmax, void* stream) {
   g_last_launches = 0;
@@ -277,6 +464,44 @@ I8_API i8_status f16_matmul(const void* X, int T, int in, const void* W, int out
   return st;
 }
 
+I8_API i8_status f16_ffn(const void* X, int T, int d_model, int d_ff, const void* W_up,
+                         const void* bias_up, const void* W_down, const void* bias_down,
+                         int act, void* H, void* Y, void* stream) {
+  g_last_launches = 0;
+  if (act != I8_ACT_NONE && act != I8_ACT_RELU) return I8_ERR_INVALID_ARG;
+  if (T < 0 || d_model <= 0 || d_ff <= 0 || !W_up || !W_down) return I8_ERR_INVALID_ARG;
+  if (T > 0 && (!X || !H || !Y)) return I8_ERR_INVALID_ARG;
+  if (d_model % 16 != 0 || d_ff % 16 != 0) return I8_ERR_ALIGNMENT;
+  if (!aligned16(X) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(H) ||
+      !aligned16(Y) || (bias_up && !aligned16(bias_up)) || (bias_down && !aligned16(bias_down)))
+    return I8_ERR_ALIGNMENT;
+  if (T == 0) return I8_OK;
+  i8_status st = check_device();
+  if (st != I8_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmArgs g;
+  g.a_f16 = W_up;
+  g.b_f16 = X;
+  g.bias = bias_up;
+  g.Y = H;
+  g.T = T;
+  g.in = d_model;
+  g.out = d_ff;
+  g.relu = act == I8_ACT_RELU ? 1 : 0;
+  if ((st = from_cuda(launch_f16_gemm(g, s))) != I8_OK) return st;
+  GemmArgs g2;
+  g2.a_f16 = W_down;
+  g2.b_f16 = H;
+  g2.bias = bias_down;
+  g2.Y = Y;
+  g2.T = T;
+  g2.in = d_ff;
+  g2.out = d_model;
+  if ((st = from_cuda(launch_f16_gemm(g2, s))) != I8_OK) return st;
+  g_last_launches = 2;
+  return I8_OK;
+}
+
 I8_API i8_status i8_get_status(const void* workspace, void* stream) {
   if (!workspace) return I8_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -304,7 +529,10 @@ I8_API const char* i8_status_string(i8_status s) {
 
 I8_API int i8_last_launch_count(void) { return g_last_launches; }
 
-I8_API void i8_set_profile_events(void** events) {
-  for (int i = 0; i < 4; ++i)
-    g_prof[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+I8_API void i8_set_profile_events_n(void** events, int n) {
+  g_prof_n = (events && n > 0) ? std::min(n, kProfSlots) : 0;
+  for (int i = 0; i < kProfSlots; ++i)
+    g_prof[i] = i < g_prof_n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
 }
+
+I8_API void i8_set_profile_events(void** events) { i8_set_profile_events_n(events, 4); }

@@ -15,6 +15,9 @@
 // its flags into the 32-column mask words with one atomicOr per non-zero word; the last
 // CTA to arrive turns the mask into the ascending index list (block scan of per-word
 // popcounts), so the order never depends on scheduling.
+//
+// When the matmul that produced X already ORed its columns' flags into the mask (its
+// epilogue sees every output value once), mask_index_kernel does only the compaction.
 #include "int8mm_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -36,6 +39,47 @@ __device__ __forceinline__ void fold_absmax(uint32_t (&m)[4], const uint4& v) {
   m[1] = __vmaxu2(m[1], v.y & 0x7fff7fffu);
   m[2] = __vmaxu2(m[2], v.z & 0x7fff7fffu);
   m[3] = __vmaxu2(m[3], v.w & 0x7fff7fffu);
+}
+
+// Block-wide compaction (kColThreads threads): the set bits of mask[0, words) become the
+// ascending column list idx[0, n); hdr gets n, min(n, ncap) and, past the capacity,
+// I8_ERR_OUTLIER_CAP. Each thread takes a contiguous run of words; a block scan of their
+// popcounts gives every run its output position, so the order never depends on timing.
+__device__ void compact_mask(const uint32_t* mask, int words, int32_t* idx, WsHeader* hdr,
+                             int ncap, int* s_warp_sum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (words + kColThreads - 1) / kColThreads;
+  const int w0 = min(words, threadIdx.x * per), w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(__ldcg(&mask[w]));
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kColThreads / 32; ++w) {
+    before += (w < warp) ? s_warp_sum[w] : 0;
+    total += s_warp_sum[w];
+  }
+  int pos = before + incl - cnt;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = __ldcg(&mask[w]);
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      idx[pos++] = w * 32 + b;
+    }
+  }
+  if (threadIdx.x == 0) {
+    hdr->n_out = total;
+    hdr->n_out_used = min(total, ncap);
+    if (total > ncap) atomicCAS(&hdr->status, 0, (int)I8_ERR_OUTLIER_CAP);
+  }
 }
 
 __global__ void __launch_bounds__(kColThreads) colstats_kernel(
@@ -99,39 +143,19 @@ __global__ void __launch_bounds__(kColThreads) colstats_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  compact_mask(mask, words, idx, hdr, ncap, s_warp_sum);
+}
 
-  const int per = (words + kColThreads - 1) / kColThreads;
-  const int w0 = min(words, threadIdx.x * per), w1 = min(words, w0 + per);
-  int cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(__ldcg(&mask[w]));
-  int incl = cnt;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
+// One CTA of kColThreads: mask words -> ascending column list, count, capacity check.
+__global__ void __launch_bounds__(kColThreads) mask_index_kernel(
+    WsHeader* hdr, const uint32_t* mask, int32_t* idx, int words, int ncap,
+    const WsHeader* prev) {
+  __shared__ int s_warp_sum[kColThreads / 32];
+  if (prev && threadIdx.x == 0) {
+    const int ps = *reinterpret_cast<volatile const int*>(&prev->status);
+    if (ps != 0) atomicCAS(&hdr->status, 0, ps);
   }
-  if (lane == 31) s_warp_sum[warp] = incl;
-  __syncthreads();
-  int before = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kColThreads / 32; ++w) {
-    before += (w < warp) ? s_warp_sum[w] : 0;
-    total += s_warp_sum[w];
-  }
-  int pos = before + incl - cnt;
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = __ldcg(&mask[w]);
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      idx[pos++] = w * 32 + b;
-    }
-  }
-  if (threadIdx.x == 0) {
-    hdr->n_out = total;
-    hdr->n_out_used = min(total, ncap);
-    if (total > ncap) atomicCAS(&hdr->status, 0, (int)I8_ERR_OUTLIER_CAP);
-  }
+  compact_mask(mask, words, idx, hdr, ncap, s_warp_sum);
 }
 
 uint16_t threshold_to_half_bits(float threshold) {
@@ -154,6 +178,12 @@ cudaError_t launch_colstats(const void* X, int T, int in, uint16_t thr_bits, WsH
   colstats_kernel<<<grid, kColThreads, 0, s>>>(static_cast<const uint16_t*>(X), T, in,
                                                 rows_per_split, thr_bits, hdr, mask, idx,
                                                 (in + 31) / 32, ncap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_index(int in, WsHeader* hdr, uint32_t* mask, int32_t* idx, int ncap,
+                              const WsHeader* prev, cudaStream_t s) {
+  mask_index_kernel<<<1, kColThreads, 0, s>>>(hdr, mask, idx, (in + 31) / 32, ncap, prev);
   return cudaGetLastError();
 }
 

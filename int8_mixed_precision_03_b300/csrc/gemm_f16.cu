@@ -7,7 +7,8 @@
 // A = W fp16 [out, in] and B = X fp16 [T, in], both by TMA with the 128-byte swizzle,
 // K-major, read by the MMA from shared memory. Two accumulators (2 x BN TMEM columns)
 // alternate between tiles, so the epilogue of one tile overlaps the MMAs of the next.
-// Epilogue: fp16(acc + bias[o]) staged per warp in shared memory, written by TMA stores.
+// Epilogue: fp16(acc + bias[o]), optionally through ReLU (the fp16 FFN block), staged per
+// warp in shared memory, written by TMA stores.
 //
 // Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
 // warps 4-7 epilogue. Persistent CTAs, one per SM, tiles token-block fastest.
@@ -44,6 +45,7 @@ struct ParamsF {
   int y_tma;
   const uint16_t* bias;
   uint16_t* Y;
+  int relu;  // ReLU on Y (the fp16 FFN's up projection)
   uint64_t timeout_ns;
 };
 
@@ -161,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t yh[kW / 2];
 #pragma unroll
         for (int j = 0; j < kW; ++j) {
-          const uint32_t h = __half_as_ushort(__float2half_rn(__uint_as_float(f[j]) + bo));
+          float v = __uint_as_float(f[j]) + bo;
+          if (p.relu) v = fmaxf(v, 0.0f);
+          const uint32_t h = __half_as_ushort(__float2half_rn(v));
           yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
         }
         box_reuse_wait(lane);
@@ -208,6 +212,7 @@ cudaError_t launch_f16_bn(const GemmArgs& a, cudaStream_t s) {
   p.y_tma = y_tma ? 1 : 0;
   p.bias = static_cast<const uint16_t*>(a.bias);
   p.Y = static_cast<uint16_t*>(a.Y);
+  p.relu = a.relu;
   p.timeout_ns = a.timeout_ns;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < kSmCount ? tiles : kSmCount;

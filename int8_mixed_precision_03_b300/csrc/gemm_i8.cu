@@ -32,6 +32,11 @@
 // of its tile is folded into it, and the tile's last segment reads it back.
 // Epilogue: Y[t, o] = fp16(acc * rowabs[t] * SCB[o] / 127^2 + outlier + bias[o]), staged
 // per warp in shared memory (two boxes of tokens x 32 features) and written by TMA stores.
+// When Y is the input of a following int8 matmul (an FFN's up projection), the epilogue
+// also applies the activation (ReLU or none) and computes that matmul's outlier flags:
+// each lane owns one column of Y, keeps the largest fp16 magnitude over the tile's valid
+// tokens, and the warp ORs one 32-column mask word per tile (step 1 of the next matmul
+// without reading Y again).
 //
 // Warp roles (512 threads): warp 0 TMA for B, warp 1 MMA issuer and TMEM owner, warp 2 TMA
 // for the weight stream, warps 4-7 and 12-15 converters, warps 8-11 epilogue (warp w
@@ -87,9 +92,15 @@ struct Params {
   const uint16_t* bias;
   uint16_t* Y;
   int32_t* acc_debug;
+  uint32_t* next_mask;        // FFN up projection: the next matmul's outlier mask
+  uint32_t next_thr;          // its threshold as fp16 magnitude bits
+  int next_relu;              // ReLU on Y before the statistics
   uint64_t timeout_ns;
   int debug_skip_loads;
 };
+
+// Epilogue variants: plain, plain + int32 export, activation + next matmul's column flags.
+enum EpiMode { kEpiPlain = 0, kEpiDebug = 1, kEpiNext = 2 };
 
 __device__ __forceinline__ int outlier_kblocks(const Params& p) {
   const int n = *reinterpret_cast<volatile const int*>(&p.hdr->n_out_used);
@@ -125,13 +136,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, bool kDebug>
+template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmWo, const __grid_constant__ CUtensorMap tmXo,
                    const __grid_constant__ CUtensorMap tmY, const Params p) {
   using C = Cfg<BN>;
   constexpr int kS = C::kStages, kS8 = C::kStages8, kW = C::kW;
+  constexpr bool kDebug = kMode == kEpiDebug, kNext = kMode == kEpiNext;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + C::bars);
@@ -387,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nseg_int = count_int_segments(p, n_blk);
       const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
+      uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
       for (int si = 0; si < nseg_tile && ok; ++si, ++nseg) {
         const bool is_out = si >= nseg_int;
         const bool first = si == 0;
@@ -454,8 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
               }
               const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
-              const float y = (float)acc * (rj * so) + fo + bo;
+              float y = (float)acc * (rj * so) + fo + bo;
+              if constexpr (kNext) {
+                if (p.next_relu) y = fmaxf(y, 0.0f);
+              }
               const uint32_t h = __half_as_ushort(__float2half_rn(y));
+              if constexpr (kNext) {
+                if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
+              }
               yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
               if constexpr (kDebug) pc[j] = acc;
             }
@@ -475,6 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
             }
           }
+          if constexpr (kNext) {  // the tile's flags of columns m0 + 32q .. + 31
+            const uint32_t word = __ballot_sync(0xffffffffu, o_ok && ymax >= p.next_thr);
+            if (lane == 0 && word != 0u) atomicOr(&p.next_mask[(m0 + 32 * q) >> 5], word);
+          }
         }
       }
     }
@@ -488,15 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int BN, bool kDebug>
+template <int BN, int kMode>
 cudaError_t launch_kernel(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
                           const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
                           const Params& p, int grid) {
   using C = Cfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kDebug>,
+  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
   if (e != cudaSuccess) return e;
-  i8_gemm_kernel<BN, kDebug><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
+  i8_gemm_kernel<BN, kMode><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
   return cudaGetLastError();
 }
 
@@ -539,12 +562,18 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.bias = static_cast<const uint16_t*>(a.bias);
   p.Y = static_cast<uint16_t*>(a.Y);
   p.acc_debug = a.acc_debug;
+  p.next_mask = a.next.mask;
+  p.next_thr = a.next.thr_bits;
+  p.next_relu = a.next.relu;
   p.timeout_ns = a.timeout_ns;
   p.debug_skip_loads = a.debug_skip_loads;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < kSmCount ? tiles : kSmCount;
-  if (a.acc_debug) return launch_kernel<BN, true>(s, mA8, mB, mWo, mXo, mY, p, grid);
-  return launch_kernel<BN, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  // ReLU comes only with the statistics epilogue (an FFN's up projection)
+  if ((a.next.relu && !a.next.mask) || (a.next.mask && a.acc_debug)) return cudaErrorInvalidValue;
+  if (a.next.mask) return launch_kernel<BN, kEpiNext>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  if (a.acc_debug) return launch_kernel<BN, kEpiDebug>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  return launch_kernel<BN, kEpiPlain>(s, mA8, mB, mWo, mXo, mY, p, grid);
 }
 
 }  // namespace

@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(GvShape<T>::kThreads, 1) gemv_i8_kernel(
     const int8_t* __restrict__ xq, const float* __restrict__ rowabs,
     const WsHeader* __restrict__ hdr, const int32_t* __restrict__ idx,
     const uint16_t* __restrict__ xout, int ncap, const uint16_t* __restrict__ bias,
-    uint16_t* __restrict__ Y, int32_t* __restrict__ acc_debug, int use_tab) {
+    uint16_t* __restrict__ Y, int32_t* __restrict__ acc_debug, int use_tab,
+    const NextLayer next) {
   // shared memory: x codes [T][in] | outlier bytes [rows of this CTA][kOutTab] |
   //                X_out [T][kOutTab] fp32
   constexpr int kGvThreads = GvShape<T>::kThreads, kGvWarps = GvShape<T>::kWarps;
@@ -207,8 +208,14 @@ __global__ void __launch_bounds__(GvShape<T>::kThreads, 1) gemv_i8_kernel(
       }
       const float so = scb * (1.0f / 16129.0f);
       const float bo = bias ? __half2float(__ushort_as_half(__ldg(&bias[o]))) : 0.0f;
-      const float y = (float)a * (ra_l * so) + fo + bo;
-      Y[(size_t)lt * out + o] = __half_as_ushort(__float2half_rn(y));
+      float y = (float)a * (ra_l * so) + fo + bo;
+      if (next.relu) y = fmaxf(y, 0.0f);
+      const uint32_t h = __half_as_ushort(__float2half_rn(y));
+      Y[(size_t)lt * out + o] = (uint16_t)h;
+      // FFN up projection: flag column o of Y for the next matmul (at most T atomics
+      // per flagged column)
+      if (next.mask && (h & 0x7fffu) >= next.thr_bits)
+        atomicOr(&next.mask[o >> 5], 1u << (o & 31));
       if (acc_debug) acc_debug[(size_t)lt * out + o] = a;
     }
   }
@@ -233,7 +240,7 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t s) {
   gemv_i8_kernel<T><<<kSmCount, GvShape<T>::kThreads, smem, s>>>(
       a.CB, a.SCB, a.in, a.out, a.xq8, a.rowabs, a.hdr, a.idx,
       static_cast<const uint16_t*>(a.xout), a.ncap, static_cast<const uint16_t*>(a.bias),
-      static_cast<uint16_t*>(a.Y), a.acc_debug, use_tab ? 1 : 0);
+      static_cast<uint16_t*>(a.Y), a.acc_debug, use_tab ? 1 : 0, a.next);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,20 @@ uint16_t threshold_to_half_bits(float threshold);
 // ---- kernel launchers (each returns cudaGetLastError() of its launch)
 cudaError_t launch_colstats(const void* X, int T, int in, uint16_t thr_bits, WsHeader* hdr,
                             uint32_t* mask, int32_t* idx, int ncap, cudaStream_t s);
+// Column statistics already in the mask (ORed by the previous matmul's epilogue): one CTA
+// turns the mask into the ordered index list and the count. A non-null `prev` status
+// word is carried into hdr->status first, so a chain reports its first error in one word.
+cudaError_t launch_mask_index(int in, WsHeader* hdr, uint32_t* mask, int32_t* idx, int ncap,
+                              const WsHeader* prev, cudaStream_t s);
+
+// Optional epilogue work of a matmul whose output feeds another int8 matmul: ReLU on Y,
+// and the next matmul's outlier mask (one bit per column of Y) ORed with the columns where
+// some valid token has |fp16 y| >= the next threshold (compared as fp16 magnitude bits).
+struct NextLayer {
+  int relu = 0;
+  uint32_t* mask = nullptr;      // null: no statistics
+  uint32_t thr_bits = 0x7C00u;
+};
 cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* CB,
                                    const float* SCB, int out, const WsHeader* hdr,
                                    const uint32_t* mask, const int32_t* idx, int ncap,
@@ -102,6 +116,8 @@ struct GemmArgs {
   void* Y = nullptr;
   int32_t* acc_debug = nullptr; // optional [T, out] int32 export
   int T = 0, in = 0, out = 0;
+  NextLayer next;               // int8 path: ReLU + next layer's column statistics
+  int relu = 0;                 // fp16 comparator: ReLU on Y
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)
 };
@@ -124,6 +140,7 @@ struct GemvArgs {
   const void* bias = nullptr;
   void* Y = nullptr;
   int32_t* acc_debug = nullptr;
+  NextLayer next;
 };
 bool gemv_fits(int T, int in);                            // either decode kernel applies
 cudaError_t launch_gemv_i8(const GemvArgs& a, cudaStream_t s);  // dispatches on T

@@ -123,3 +123,51 @@ def test_stall_hook_rejects_decode_sizes_and_a_zero_limit_before_any_launch():
     assert L.i8_test_stalled_matmul(p, 8, 256, p, p, 64, p, p, 1 << 30, 1000, None) == 1
     assert L.i8_test_stalled_matmul(p, 64, 256, p, p, 64, p, p, 1 << 30, 0, None) == 1
     assert L.i8_last_launch_count() == 0
+
+
+def test_ffn_workspace_size_is_both_matmuls(L):
+    f, g = L.int8_ffn_workspace_size, L.int8_matmul_workspace_size
+    T, d, dff = 200, 256, 1024
+    both = g(T, dff, d, 0) + g(T, d, dff, 0)
+    # the two sections are 256-byte aligned and each is a multiple of 256 bytes
+    assert f(T, d, dff, 0) == both
+    assert f(T, d, dff, 64) == g(T, dff, d, 64) + g(T, d, dff, 64)
+    assert f(T, d, dff, 1) == f(T, d, dff, 64)
+    # the capacity of each matmul is clamped to its own input width
+    assert f(T, d, dff, 512) == g(T, dff, d, 512) + g(T, d, dff, 256)
+    assert f(-1, d, dff, 0) == 0 and f(T, 0, dff, 0) == 0 and f(T, d, 0, 0) == 0
+    assert f(T, d, 262144, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(act=2), 1),                  # unknown activation
+    (dict(act=-1), 1),
+    (dict(Y=None), 1),
+    (dict(CBd=None), 1),
+    (dict(dff=24), 2),                 # d_ff not a multiple of 16
+    (dict(d=40), 2),                   # d_model not a multiple of 16
+    (dict(CBd=A + 8), 2),
+    (dict(bd=A + 2), 2),
+    (dict(Y=A + 4), 2),
+    (dict(threshold=0.0), 1),
+    (dict(ws_bytes=1024), 3),
+    (dict(T=0), 0),                    # a no-op: nothing launched, no device needed
+])
+def test_ffn_host_validation(L, kw, code):
+    a = dict(X=A, T=16, d=256, dff=1024, CBu=A, SCBu=A, bu=None, CBd=A, SCBd=A, bd=None,
+             threshold=6.0, act=1, H=A, Y=A, ws=A, ws_bytes=1 << 30)
+    a.update(kw)
+    p = lambda v: fake(v) if v else None  # noqa: E731
+    r = L.int8_ffn(p(a["X"]), a["T"], a["d"], a["dff"], p(a["CBu"]), p(a["SCBu"]), p(a["bu"]),
+                   p(a["CBd"]), p(a["SCBd"]), p(a["bd"]), a["threshold"], a["act"], p(a["H"]),
+                   p(a["Y"]), p(a["ws"]), a["ws_bytes"], None)
+    assert r == code
+    assert L.i8_last_launch_count() == 0
+
+
+def test_f16_ffn_validation(L):
+    p = fake(A)
+    assert L.f16_ffn(p, 4, 32, 64, p, None, p, None, 3, p, p, None) == 1
+    assert L.f16_ffn(p, 4, 32, 40, p, None, p, None, 1, p, p, None) == 2
+    assert L.f16_ffn(p, 4, 32, 64, p, None, p, None, 1, p, None, None) == 1
+    assert L.f16_ffn(p, 0, 32, 64, p, None, p, None, 1, p, p, None) == 0
