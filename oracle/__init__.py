@@ -7,6 +7,10 @@ CUDA package: the two sides only share the seeded input generators in ``synth``.
 The arithmetic lives in ``int8mm_oracle.c`` (plain C, IEEE fp32 for the quantizers, exact
 integers for the int8 products, fp64 for the output). This module is numpy marshalling.
 
+The zeropoint variant (``int8_matmul_zeropoint``) quantizes the activations' inlier columns
+per row with S and Z (the zenn summary's "Zeropoint Quantization") instead of absmax and
+adds the correction Z * (sum of the inlier weight codes) to the exact integer product.
+
 The FFN block (``ffn``) chains two of these matmuls with ReLU (or nothing) between them,
 the intermediate rounded once from fp64 to fp16 as the second matmul's input.
 
@@ -44,6 +48,9 @@ def load(path: str) -> C.CDLL:
     L.orc_int8_matmul.argtypes = [p, i64, i64, p, p, i64, C.c_float, p, p, i64, p, p, p,
                                   p, p, C.c_int]
     L.orc_int8_matmul.restype = C.c_int32
+    L.orc_int8_matmul_zp.argtypes = [p, i64, i64, p, p, i64, C.c_float, p, p, i64, p, p, p,
+                                     p, p, p, C.c_int]
+    L.orc_int8_matmul_zp.restype = C.c_int32
     L.orc_half_to_float.argtypes = [p, i64, p]
     L.orc_float_to_half.argtypes = [p, i64, p]
     L.orc_activation_to_half.argtypes = [p, i64, C.c_int, p]
@@ -171,6 +178,33 @@ def int8_matmul(X, CB, SCB, threshold=6.0, bias=None, rows=None, nthreads=None,
                               int(nthreads or default_threads()))
     return {"Y": Y, "acc": acc, "Q": Q, "rowabs": ra, "idx": idx[:n].copy(), "rows": rows}
 
+
+
+def int8_matmul_zeropoint(X, CB, SCB, threshold=6.0, bias=None, rows=None, nthreads=None,
+                          want_acc=True):
+    """The matmul with zeropoint activation codes for the selected rows of X.
+
+    Returns a dict: Y (fp64), acc (int64, codes . CB^T over all columns, outlier codes 0),
+    Q (int8), S and Z (fp32 per row), idx (outlier columns), rows."""
+    X = _f16(X)
+    T, d = X.shape
+    CB = np.ascontiguousarray(CB, dtype=np.int8)
+    SCB = np.ascontiguousarray(SCB, dtype=np.float32)
+    out = CB.shape[0]
+    assert CB.shape[1] == d
+    b = None if bias is None else _f16(bias)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    nr = rows.size
+    Y = np.empty((nr, out), np.float64)
+    acc = np.empty((nr, out), np.int64) if want_acc else None
+    Q = np.empty((nr, d), np.int8)
+    S = np.empty(nr, np.float32)
+    Z = np.empty(nr, np.float32)
+    idx = np.empty(max(d, 1), np.int32)
+    n = lib().orc_int8_matmul_zp(_ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold),
+                                 _ptr(b), _ptr(rows), nr, _ptr(Y), _ptr(acc), _ptr(Q), _ptr(S),
+                                 _ptr(Z), _ptr(idx), int(nthreads or default_threads()))
+    return {"Y": Y, "acc": acc, "Q": Q, "S": S, "Z": Z, "idx": idx[:n].copy(), "rows": rows}
 
 def activation_to_half(y: np.ndarray, relu: bool) -> np.ndarray:
     """fp16(act(y)) for fp64 y: ReLU (y <= 0 -> +0) or identity, one rounding to nearest."""

@@ -124,37 +124,46 @@ void orc_quantize_rows_absmax(const uint16_t* X, int64_t rows, int64_t cols,
   }
 }
 
-/* Zeropoint (asymmetric) row quantization, X8 = INT8(X*S - Z) with S = 254/(max-min)
- * and Z = rint(S*min) + 127, so that min maps to -127, max to +127 and 0 to the
- * integer -Z. A constant row stores S = 0, Z = min and codes 0. */
+/* Zeropoint (asymmetric) quantization of one row, X8 = INT8(X*S - Z) with
+ * S = 254/(max-min) and Z = rint(S*min) + 127, so that min maps to -127, max to +127 and 0
+ * to the integer -Z. min and max are taken over the columns not flagged in `outlier`
+ * (nullable); flagged columns get code 0. No such column: min = max = 0. A constant row
+ * stores S = 0, Z = min and codes 0. */
+static void zeropoint_row(const uint16_t* x, int64_t cols, const uint8_t* outlier, int8_t* q,
+                          float* S, float* Z) {
+  float mn = INFINITY, mx = -INFINITY;
+  int any = 0;
+  for (int64_t j = 0; j < cols; ++j) {
+    if (outlier && outlier[j]) continue;
+    float v = h2f(x[j]);
+    if (v < mn) mn = v;
+    if (v > mx) mx = v;
+    any = 1;
+  }
+  if (!any) { mn = 0.0f; mx = 0.0f; }
+  if (mx > mn) {
+    float range = mx - mn;         /* fp32 subtraction */
+    float s = 254.0f / range;      /* fp32 division */
+    float z = rintf(s * mn) + 127.0f;
+    *S = s;
+    *Z = z;
+    for (int64_t j = 0; j < cols; ++j) {
+      if (outlier && outlier[j]) { q[j] = 0; continue; }
+      float p = h2f(x[j]) * s;     /* fp32 multiply */
+      float t = p - z;             /* fp32 subtract, not fused */
+      q[j] = clamp_code(rintf(t));
+    }
+  } else {
+    *S = 0.0f;
+    *Z = mn;
+    for (int64_t j = 0; j < cols; ++j) q[j] = 0;
+  }
+}
+
 void orc_zeropoint_rows(const uint16_t* X, int64_t rows, int64_t cols, int8_t* Q, float* S,
                         float* Z) {
-  for (int64_t i = 0; i < rows; ++i) {
-    const uint16_t* x = X + i * cols;
-    float mn = INFINITY, mx = -INFINITY;
-    for (int64_t j = 0; j < cols; ++j) {
-      float v = h2f(x[j]);
-      if (v < mn) mn = v;
-      if (v > mx) mx = v;
-    }
-    if (cols == 0) { mn = 0.0f; mx = 0.0f; }
-    if (mx > mn) {
-      float range = mx - mn;         /* fp32 subtraction */
-      float s = 254.0f / range;      /* fp32 division */
-      float z = rintf(s * mn) + 127.0f;
-      S[i] = s;
-      Z[i] = z;
-      for (int64_t j = 0; j < cols; ++j) {
-        float p = h2f(x[j]) * s;     /* fp32 multiply */
-        float t = p - z;             /* fp32 subtract, not fused */
-        Q[i * cols + j] = clamp_code(rintf(t));
-      }
-    } else {
-      S[i] = 0.0f;
-      Z[i] = mn;
-      for (int64_t j = 0; j < cols; ++j) Q[i * cols + j] = 0;
-    }
-  }
+  for (int64_t i = 0; i < rows; ++i)
+    zeropoint_row(X + i * cols, cols, NULL, Q + i * cols, &S[i], &Z[i]);
 }
 
 /* FFN block intermediate: H = fp16(act(y)) for the fp64 output y of the first matmul,
@@ -185,6 +194,12 @@ typedef struct {
   const int8_t* Q;       /* [nrows, in] codes of the selected rows */
   const float* rowabs;   /* [nrows] */
   const uint16_t* Wout;  /* [out, n_out] fp16 dequantized outlier weights */
+  /* zeropoint variant (zp != 0): per selected row S and Z, per output the sum of the
+   * weight codes over the inlier columns */
+  int zp;
+  const float* rowS;
+  const float* rowZ;
+  const int64_t* cbin;
   /* outputs */
   double* Y;             /* [nrows, out] */
   int64_t* acc;          /* [nrows, out] nullable */
@@ -206,8 +221,18 @@ static void* mm_worker(void* p) {
       double f = 0.0;
       for (int32_t k = 0; k < jb->n_out; ++k)
         f += (double)h2f(x[jb->idx[k]]) * (double)h2f(jb->Wout[o * jb->n_out + k]);
-      /* dequantize: x ~ q*absmax/127 and w ~ CB*SCB/127 */
-      double y = (double)a * (double)jb->rowabs[r] * (double)jb->SCB[o] / (127.0 * 127.0);
+      double y;
+      if (!jb->zp) {
+        /* dequantize: x ~ q*absmax/127 and w ~ CB*SCB/127 */
+        y = (double)a * (double)jb->rowabs[r] * (double)jb->SCB[o] / (127.0 * 127.0);
+      } else if (jb->rowS[r] != 0.0f) {
+        /* x ~ (q + Z)/S over the inlier columns: sum_j (q_j + Z) CB_j = a + Z * cbin */
+        double az = (double)a + (double)jb->rowZ[r] * (double)jb->cbin[o];
+        y = az * (double)jb->SCB[o] / (127.0 * (double)jb->rowS[r]);
+      } else {
+        /* constant inlier row: every inlier x is Z (= min) */
+        y = (double)jb->rowZ[r] * (double)jb->cbin[o] * (double)jb->SCB[o] / 127.0;
+      }
       y += f;
       if (jb->bias) y += (double)h2f(jb->bias[o]);
       jb->Y[r * jb->out + o] = y;
@@ -230,20 +255,35 @@ void orc_outlier_weights(const int8_t* CB, const float* SCB, int64_t out, int64_
 
 /* The LLM.int8() matmul for selected rows of X:
  *   1. outlier columns of X (over all T rows);
- *   2. row-wise absmax codes of the selected rows over inlier columns (outliers -> 0);
+ *   2. row codes of the selected rows over inlier columns (outliers -> 0): absmax, or in
+ *      the zeropoint variant (zp != 0) zeropoint with S and Z per row;
  *   3. acc = codes . CB^T exactly; outlier product in fp64 from fp16 operands;
- *   4. Y = acc * rowabs * SCB / 127^2 + outlier product + bias   (fp64).
+ *   4. Y = acc * rowabs * SCB / 127^2 + outlier product + bias   (fp64), or with zeropoint
+ *      codes Y = (acc + Z * sum of the inlier weight codes) * SCB / (127 S) + ... .
  * Outputs (all caller-allocated): Y [nrows,out]; acc [nrows,out] (nullable);
- * Q [nrows,in]; rowabs [nrows]; idx [in]; returns n_out. nthreads <= 0 means 1. */
-int32_t orc_int8_matmul(const uint16_t* X, int64_t T, int64_t in, const int8_t* CB,
-                        const float* SCB, int64_t out, float threshold, const uint16_t* bias,
-                        const int64_t* rows, int64_t nrows, double* Y, int64_t* acc, int8_t* Q,
-                        float* rowabs, int32_t* idx, int nthreads) {
+ * Q [nrows,in]; rowabs [nrows] (absmax) or S, Z [nrows] (zeropoint; rowabs unused);
+ * idx [in]; returns n_out. nthreads <= 0 means 1. */
+static int32_t int8_matmul_any(const uint16_t* X, int64_t T, int64_t in, const int8_t* CB,
+                               const float* SCB, int64_t out, float threshold,
+                               const uint16_t* bias, const int64_t* rows, int64_t nrows,
+                               double* Y, int64_t* acc, int8_t* Q, float* rowabs, int zp,
+                               float* S, float* Z, int32_t* idx, int nthreads) {
   int32_t n_out = orc_outlier_columns(X, T, in, threshold, idx);
   uint8_t* mask = (uint8_t*)calloc((size_t)(in > 0 ? in : 1), 1);
   for (int32_t k = 0; k < n_out; ++k) mask[idx[k]] = 1;
-  for (int64_t r = 0; r < nrows; ++r)
-    orc_quantize_rows_absmax(X + rows[r] * in, 1, in, mask, Q + r * in, rowabs + r);
+  int64_t* cbin = NULL;
+  for (int64_t r = 0; r < nrows; ++r) {
+    if (zp)
+      zeropoint_row(X + rows[r] * in, in, mask, Q + r * in, &S[r], &Z[r]);
+    else
+      orc_quantize_rows_absmax(X + rows[r] * in, 1, in, mask, Q + r * in, rowabs + r);
+  }
+  if (zp) {
+    cbin = (int64_t*)calloc((size_t)(out > 0 ? out : 1), sizeof(int64_t));
+    for (int64_t o = 0; o < out; ++o)
+      for (int64_t j = 0; j < in; ++j)
+        if (!mask[j]) cbin[o] += CB[o * in + j];
+  }
   uint16_t* Wout = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(out * (n_out > 0 ? n_out : 1)));
   orc_outlier_weights(CB, SCB, out, in, idx, n_out, Wout);
 
@@ -253,8 +293,8 @@ int32_t orc_int8_matmul(const uint16_t* X, int64_t T, int64_t in, const int8_t* 
   mm_job* jobs = (mm_job*)calloc((size_t)nthreads, sizeof(mm_job));
   pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
   for (int t = 0; t < nthreads; ++t) {
-    mm_job j = {X, T, in, out, CB, SCB, bias, rows, nrows, idx, n_out, Q, rowabs, Wout, Y, acc,
-                out * t / nthreads, out * (t + 1) / nthreads};
+    mm_job j = {X, T, in, out, CB, SCB, bias, rows, nrows, idx, n_out, Q, rowabs, Wout,
+                zp, S, Z, cbin, Y, acc, out * t / nthreads, out * (t + 1) / nthreads};
     jobs[t] = j;
   }
   for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, mm_worker, &jobs[t]);
@@ -263,6 +303,25 @@ int32_t orc_int8_matmul(const uint16_t* X, int64_t T, int64_t in, const int8_t* 
   free(th);
   free(jobs);
   free(Wout);
+  free(cbin);
   free(mask);
   return n_out;
+}
+
+int32_t orc_int8_matmul(const uint16_t* X, int64_t T, int64_t in, const int8_t* CB,
+                        const float* SCB, int64_t out, float threshold, const uint16_t* bias,
+                        const int64_t* rows, int64_t nrows, double* Y, int64_t* acc, int8_t* Q,
+                        float* rowabs, int32_t* idx, int nthreads) {
+  return int8_matmul_any(X, T, in, CB, SCB, out, threshold, bias, rows, nrows, Y, acc, Q,
+                         rowabs, 0, NULL, NULL, idx, nthreads);
+}
+
+/* Zeropoint variant ("LLM.int8() summary" (zenn), section "Zeropoint Quantization", applied
+ * to the activations of the decomposed matmul; the weights stay CB/SCB): S and Z [nrows]. */
+int32_t orc_int8_matmul_zp(const uint16_t* X, int64_t T, int64_t in, const int8_t* CB,
+                           const float* SCB, int64_t out, float threshold, const uint16_t* bias,
+                           const int64_t* rows, int64_t nrows, double* Y, int64_t* acc,
+                           int8_t* Q, float* S, float* Z, int32_t* idx, int nthreads) {
+  return int8_matmul_any(X, T, in, CB, SCB, out, threshold, bias, rows, nrows, Y, acc, Q,
+                         NULL, 1, S, Z, idx, nthreads);
 }

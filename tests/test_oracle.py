@@ -314,3 +314,97 @@ def test_activation_rounding_is_one_step_from_fp64():
     assert h[4:].tolist() == [2048.0, 2052.0, 2050.0, 65504.0, math.inf, 1.0]
     g = oracle.activation_to_half(y, relu=False)
     assert g[0] == -3.5 and g.view(np.uint16)[1] == 0x8000 and g[4] == 2048.0
+
+
+# --------------------------------------------------------------------------- zeropoint matmul
+def zp_integer_case(outliers: bool, seed: int = 21):
+    """One-sided rows on the grid k * step (k = 0..254, every row holding 0 and 254 * step,
+    so S = 1/step and Z = 127 exactly), integer weights of absmax 127 (CB = W, SCB = 127).
+    With outliers: step 1/64 (inliers below 6) and three columns of large integers."""
+    g = np.random.default_rng(seed)
+    T, d, out = 7, 96, 40
+    step = 1.0 / 64 if outliers else 1.0
+    K = g.integers(0, 255, (T, d))
+    K[:, 3], K[:, 10] = 0, 254
+    X = K * step
+    cols = []
+    if outliers:
+        cols = [17, 50, 95]
+        X[:, cols] = g.integers(8, 61, (T, 3)) * np.where(g.random((T, 3)) < 0.5, -1, 1)
+    W = g.integers(-127, 128, (out, d))
+    W[np.arange(out), (np.arange(out) * 7) % d] = 127
+    return X.astype(np.float16), W.astype(np.float16), K, cols, step
+
+
+@pytest.mark.parametrize("outliers", [False, True])
+def test_zeropoint_matmul_on_one_sided_grid_rows_is_exact(outliers):
+    """Rows on the grid fill the full code range [-127, 127] exactly (codes k - 127, the
+    range absmax would halve on one-sided data), and the correction Z * sum(CB) restores
+    the product: Y equals X W^T exactly (dyadic rationals, exact in fp64)."""
+    X, W, K, cols, step = zp_integer_case(outliers)
+    thr = 6.0 if outliers else math.inf
+    CB, SCB = oracle.quantize_weight(W)
+    assert (SCB == 127).all()
+    r = oracle.int8_matmul_zeropoint(X, CB, SCB, threshold=thr)
+    assert r["idx"].tolist() == cols
+    assert (r["S"] == np.float32(1.0 / step)).all() and (r["Z"] == 127).all()
+    inl = np.ones(X.shape[1], bool)
+    inl[cols] = False
+    np.testing.assert_array_equal(r["Q"][:, inl].astype(np.int64), K[:, inl] - 127)
+    assert not r["Q"][:, ~inl].any()
+    np.testing.assert_array_equal(r["acc"], r["Q"].astype(np.int64) @ CB.astype(np.int64).T)
+    exact = X.astype(np.float64) @ W.astype(np.float64).T
+    np.testing.assert_array_equal(r["Y"], exact)
+    if not outliers:  # absmax on the same rows uses half the code range and is not exact
+        ra = oracle.int8_matmul(X, CB, SCB, threshold=thr)
+        assert not np.array_equal(ra["Y"], exact)
+
+
+def test_zeropoint_matmul_constant_and_all_outlier_rows():
+    """A constant inlier row dequantizes to its value (S = 0, Z = min); when every column is
+    an outlier column the int8 part is empty and Y is the fp16 outlier product."""
+    X, W, K, cols, step = zp_integer_case(True)
+    X[2, :] = np.float16(0.5)
+    X[2, cols] = np.float16(9)
+    CB, SCB = oracle.quantize_weight(W)
+    bias = np.arange(W.shape[0], dtype=np.float16) * np.float16(0.25)
+    r = oracle.int8_matmul_zeropoint(X, CB, SCB, 6.0, bias)
+    assert r["S"][2] == 0 and r["Z"][2] == 0.5 and not r["Q"][2].any()
+    exact = X.astype(np.float64) @ W.astype(np.float64).T + bias.astype(np.float64)
+    np.testing.assert_array_equal(r["Y"], exact)
+    Xa = np.full((3, 32), 7, np.float16)
+    Xa[1] = -11
+    Wa = np.tile(np.arange(-16, 16, dtype=np.float16), (5, 1))
+    CBa, SCBa = oracle.quantize_weight(Wa)
+    ra = oracle.int8_matmul_zeropoint(Xa, CBa, SCBa, 6.0)
+    assert ra["idx"].size == 32 and (ra["S"] == 0).all() and (ra["Z"] == 0).all()
+    Wo = oracle.outlier_weights(CBa, SCBa, ra["idx"]).astype(np.float64)
+    np.testing.assert_array_equal(ra["Y"], Xa.astype(np.float64) @ Wo.T)
+
+
+def test_zeropoint_matmul_within_quantization_error_bound():
+    """Synthetic tiny workload: |Y - X W^T| <= sum_j |w_j| / S (+ the weight and outlier
+    weight rounding terms of the absmax bound), and the zeropoint codes of a row are the
+    standalone zeropoint quantizer's codes of its inlier columns."""
+    w = synth.WORKLOADS["tiny"]
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    CB, SCB = oracle.quantize_weight(W)
+    r = oracle.int8_matmul_zeropoint(X, CB, SCB, threshold=w.threshold, bias=bias)
+    inl = np.ones(X.shape[1], bool)
+    inl[r["idx"]] = False
+    Qs, Ss, Zs = oracle.zeropoint_rows(np.ascontiguousarray(X[:, inl]))
+    np.testing.assert_array_equal(r["Q"][:, inl], Qs)
+    np.testing.assert_array_equal(r["S"], Ss)
+    np.testing.assert_array_equal(r["Z"], Zs)
+    exact = X.astype(np.float64) @ W.astype(np.float64).T + bias.astype(np.float64)
+    Xf, Wf = X.astype(np.float64), W.astype(np.float64)
+    # activation error: half a step, a whole step where the clamp at -127 / 127 binds
+    ex = 1.0 / r["S"].astype(np.float64) * (1 + 1e-6) + 1e-9
+    ew = SCB.astype(np.float64) * (1.0 / 254 + 2.0**-22)
+    Xa, Wa = np.abs(Xf), np.abs(Wf)
+    b = (Xa[:, inl].sum(1)[:, None] * ew[None, :] + ex[:, None] * Wa[:, inl].sum(1)[None, :]
+         + inl.sum() * ex[:, None] * ew[None, :])
+    idx = r["idx"]
+    wout = np.abs(Wf[:, idx]) + ew[:, None]
+    b += Xa[:, idx] @ (ew[:, None] + wout * 2.0**-11 + 2.0**-25).T
+    assert (np.abs(r["Y"] - exact) <= b * (1 + 1e-9) + 1e-12).all()

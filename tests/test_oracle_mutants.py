@@ -14,7 +14,9 @@ SRC = obuild.SRC
 # (name, original text, planted mistake)
 MUTANTS = [
     ("threshold strictly greater", ">= threshold) hit = 1", "> threshold) hit = 1"),
-    ("absmax includes outlier columns", "if (outlier && outlier[j]) continue;", ";"),
+    ("absmax includes outlier columns",
+     "if (outlier && outlier[j]) continue;\n      float v = fabsf(",
+     ";\n      float v = fabsf("),
     ("dequantize by 127 not 127^2", "/ (127.0 * 127.0)", "/ 127.0"),
     ("outlier product dropped", "y += f;", "y += 0.0 * f;"),
     ("weight row stride transposed", "jb->CB + o * jb->in", "jb->CB + o"),
@@ -27,6 +29,16 @@ MUTANTS = [
     ("ReLU mirrors negatives", "if (relu && !(v > 0.0)) v = 0.0;",
      "if (relu && !(v > 0.0)) v = -v;"),
     ("intermediate rounded twice", "_Float16 t = (_Float16)v;", "_Float16 t = (_Float16)(float)v;"),
+    ("zeropoint correction dropped",
+     "double az = (double)a + (double)jb->rowZ[r] * (double)jb->cbin[o];",
+     "double az = (double)a;"),
+    ("zeropoint correction over outlier columns too", "if (!mask[j]) cbin[o] += CB[o * in + j];",
+     "cbin[o] += CB[o * in + j];"),
+    ("zeropoint scale inverted", "/ (127.0 * (double)jb->rowS[r])",
+     "* (double)jb->rowS[r] / 127.0"),
+    ("zeropoint range over outlier columns",
+     "if (outlier && outlier[j]) continue;\n    float v = h2f(x[j]);",
+     ";\n    float v = h2f(x[j]);"),
 ]
 
 PIN_TESTS = [
@@ -42,6 +54,9 @@ PIN_TESTS = [
     lambda: pins.test_integer_ffn_block_reduces_to_exact_integer_chain(True),
     pins.test_ffn_without_activation_is_two_chained_matmuls,
     pins.test_activation_rounding_is_one_step_from_fp64,
+    lambda: pins.test_zeropoint_matmul_on_one_sided_grid_rows_is_exact(True),
+    pins.test_zeropoint_matmul_constant_and_all_outlier_rows,
+    pins.test_zeropoint_matmul_within_quantization_error_bound,
 ]
 
 
