@@ -13,8 +13,9 @@ is bracketed by a barrier and a device synchronize, and the time is the max over
 The reference arm (`--impl reference`) is the CPU oracle on the host cores, timed on a
 bounded sample of rows of the same workload.
 
-Prints one JSON line (rank 0). `--all` prints one line per configuration, then the FFN
-block line (`--ffn` alone prints only that one) and the standalone row quantizers.
+Prints one JSON line (rank 0). `--all` prints one line per configuration, the 6.7B line
+with zeropoint activation codes (`--zeropoint`), the FFN block line (`--ffn` alone prints
+only that one) and the standalone row quantizers.
 """
 from __future__ import annotations
 
@@ -125,11 +126,12 @@ def hbm_bound(w: synth.Workload) -> bool:
     return w.T <= 64
 
 
-def roofline(w: synth.Workload, matmul_ms: float, peaks: dict, peak_src: str) -> dict:
+def roofline(w: synth.Workload, matmul_ms: float, peaks: dict, peak_src: str,
+             zeropoint: bool = False) -> dict:
     """Roofline of the dominant kernel (the matmul), from its CUDA-event time."""
     s = matmul_ms / 1e3
-    kernel = matmul_kernel(w)
-    traffic = measured_traffic(w.name, kernel)
+    kernel = "i8_gemm_kernel" if zeropoint else matmul_kernel(w)
+    traffic = None if zeropoint else measured_traffic(w.name, kernel)
     if hbm_bound(w):
         achieved = matmul_bytes(w) / s / 1e9
         peak = float(peaks["hbm_gbs"])
@@ -333,9 +335,18 @@ def run_ours(args) -> None:
     ws = i8.alloc_workspace(w.T, w.d_in, w.d_out, device)
     Y = torch.empty((w.T, w.d_out), dtype=torch.float16, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    zp = args.zeropoint
+    if zp:   # zeropoint activation codes; the weight's code sums are prepared with CB
+        sums = i8.int8_weight_code_sums(CB)
+
+    def matmul(x, y, wsp):
+        if zp:
+            i8.int8_matmul_zeropoint(x, CB, SCB, sums, w.threshold, bias, Y=y, workspace=wsp)
+        else:
+            i8.int8_matmul(x, CB, SCB, w.threshold, bias, Y=y, workspace=wsp)
 
     def step():
-        i8.int8_matmul(X, CB, SCB, w.threshold, bias, Y=Y, workspace=ws)
+        matmul(X, Y, ws)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -403,7 +414,7 @@ def run_ours(args) -> None:
             b = k % nbuf
             with torch.cuda.stream(streams[b]):
                 Xe[b].copy_(Xpin, non_blocking=True)
-                i8.int8_matmul(Xe[b], CB, SCB, w.threshold, bias, Y=Ye[b], workspace=wse[b])
+                matmul(Xe[b], Ye[b], wse[b])
                 Ype[b].copy_(Ye[b], non_blocking=True)
         for st in streams:
             start.wait_stream(st)
@@ -439,13 +450,15 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    roof = roofline(w, statistics.mean(k_ms["matmul"]), peaks, peak_src)
+    roof = roofline(w, statistics.mean(k_ms["matmul"]), peaks, peak_src, zp)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": METRIC.replace("int8_matmul", "int8_matmul_zeropoint") if zp else METRIC,
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_s / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d_in": w.d_in, "d_out": w.d_out,
                    "threshold": w.threshold, "n_outlier_cols": w.n_outlier_cols,
+                   "activation_codes": "zeropoint" if zp else "absmax",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between timed steps (256 MiB write, untimed)"},
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
@@ -462,7 +475,7 @@ def run_ours(args) -> None:
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not zp:
         import oracle
         CBo, SCBo = oracle.quantize_weight(Wh)
         line["cpu_baseline"] = cpu_baseline_sample(w, Xh, CBo, SCBo, bh, os.cpu_count() or 1)
@@ -686,6 +699,8 @@ def main(argv=None) -> None:
     ap.add_argument("--all", action="store_true",
                     help="one line per configuration (1 GPU, no CPU baseline)")
     ap.add_argument("--ffn", action="store_true", help="only the FFN block line (1 GPU)")
+    ap.add_argument("--zeropoint", action="store_true",
+                    help="zeropoint activation codes (int8_matmul_zeropoint)")
     ap.add_argument("--ffn-workload", default=DEFAULT_FFN, choices=sorted(synth.FFN_WORKLOADS))
     args = ap.parse_args(argv)
     if args.impl == "reference":
@@ -697,6 +712,9 @@ def main(argv=None) -> None:
         for name in ALL_CONFIGS:
             args.workload = name
             run_ours(args)
+        args.workload, args.zeropoint = DEFAULT_WORKLOAD, True
+        run_ours(args)
+        args.zeropoint = False
         run_ffn(args)
         run_rows(args)
     elif args.ffn:

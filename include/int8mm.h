@@ -144,6 +144,47 @@ i8_status zeropoint_quantize_rows(const void* X, int rows, int cols, int8_t* Q, 
 i8_status f16_matmul(const void* X, int T, int in, const void* W, int out, const void* bias,
                      void* Y, void* stream);
 
+/*
+ * Sums of each weight row's int8 codes, CBsum[o] = sum_j CB[o, j] (int32 [out]): the
+ * per-weight input of int8_matmul_zeropoint, computed once with the codes. One launch.
+ */
+i8_status int8_weight_code_sums(const int8_t* CB, int out, int in, int32_t* CBsum,
+                                void* stream);
+
+/*
+ * The matmul with zeropoint activation codes ("LLM.int8() summary" (zenn), section
+ * "Zeropoint Quantization": X8 = INT8(X16*S - Z), X16 = (X8 + Z)/S, S = 254/(max - min),
+ * which uses the whole code range on one-sided rows such as ReLU outputs; "Hugging Face,
+ * LLM.int8() ..." (agentlenshq), section "zeropoint vs absmax").
+ * Outlier columns are found and multiplied in fp16 exactly as in int8_matmul. Each row's
+ * inlier columns are quantized with S = 254/(max - min), Z = rint(S*min) + 127 (min, max
+ * over the inlier columns; none: 0, 0), code = clamp(rint(x*S - Z), -127, 127); a row
+ * without spread has S = 0, Z = min and codes 0. The weights stay CB/SCB (absmax), so
+ *   Y = (acc + Z * sum_{inlier j} CB[o,j]) * SCB[o] / (127 S) + outlier product + bias,
+ * acc the exact int32 code product, the correction exact in 64-bit integers; a row without
+ * spread contributes Z * sum_{inlier j} CB[o,j] * SCB[o] / 127.
+ *   CBsum : int32 [out] from int8_weight_code_sums(CB)
+ * Other arguments, the workspace (int8_matmul_workspace_size) and the errors are those of
+ * int8_matmul. Every T runs on the tensor-core kernel (no decode-kernel variant).
+ * Launches: one memset and three kernels.
+ */
+i8_status int8_matmul_zeropoint(const void* X, int T, int in, const int8_t* CB,
+                                const float* SCB, const int32_t* CBsum, int out,
+                                float threshold, const void* bias, void* Y, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * int8_matmul_zeropoint plus its intermediates, for tests (each extra pointer may be NULL):
+ * outlier_idx int32 [in], n_out int32 [1], Xq int8 [T, in] (outlier columns 0),
+ * S and Z fp32 [T], acc_s32 int32 [T, out] = sum_j Xq[i,j]*CB[o,j] (without the Z term).
+ */
+i8_status int8_matmul_zeropoint_debug(const void* X, int T, int in, const int8_t* CB,
+                                      const float* SCB, const int32_t* CBsum, int out,
+                                      float threshold, const void* bias, void* Y,
+                                      void* workspace, size_t ws_bytes, void* stream,
+                                      int32_t* outlier_idx, int32_t* n_out, int8_t* Xq,
+                                      float* S, float* Z, int32_t* acc_s32);
+
 /* Activation between the two matmuls of int8_ffn / f16_ffn. */
 #define I8_ACT_NONE 0
 #define I8_ACT_RELU 1
@@ -247,7 +288,7 @@ int i8_last_launch_count(void);
  * which loads this library reserves until the process exits. Sizes whose workspace (with a
  * 64-column outlier capacity) does not fit return I8_ERR_SCRATCH_LIMIT before any launch;
  * within the limit the outlier capacity is the largest multiple of 64 columns that fits.
- * Roughly: 2*T*in + 128*(T + out) + 4*in + 75776*BN bytes plus a few KB must fit in
+ * Roughly: 2*T*in + 132*(T + out) + 4*in + 75776*BN bytes plus a few KB must fit in
  * 32 MiB, with BN the matmul's token tile (16, 32, 64, 128 or, above 128 tokens, 256).
  * - The first call on a device looks up the scratch's device address (once per device,
  *   with that device current); make that first call before any stream capture.

@@ -33,6 +33,10 @@ SIGNATURES = {
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
     "zeropoint_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p, _p]),
     "f16_matmul": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
+    "int8_weight_code_sums": (_i, [_p, _i, _i, _p, _p]),
+    "int8_matmul_zeropoint": (_i, [_p, _i, _i, _p, _p, _p, _i, _f, _p, _p, _p, _sz, _p]),
+    "int8_matmul_zeropoint_debug": (_i, [_p, _i, _i, _p, _p, _p, _i, _f, _p, _p, _p, _sz, _p,
+                                         _p, _p, _p, _p, _p, _p]),
     "int8_ffn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "int8_ffn": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _f, _i, _p, _p, _p, _sz, _p]),
     "int8_ffn_debug": (_i, [_p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _f, _i, _p, _p, _p, _sz,
@@ -213,6 +217,62 @@ def f16_matmul(X: torch.Tensor, W: torch.Tensor, bias: torch.Tensor | None = Non
     _check("f16_matmul", lib().f16_matmul(_ptr(X), T, d, _ptr(W), out, _ptr(bias), _ptr(Y),
                                           _stream(X.device)))
     return Y
+
+
+def int8_weight_code_sums(CB: torch.Tensor) -> torch.Tensor:
+    """int32 [out]: the sum of each weight row's codes (input of int8_matmul_zeropoint)."""
+    _need(CB, torch.int8, "CB")
+    out, d = CB.shape
+    sums = torch.empty(out, dtype=torch.int32, device=CB.device)
+    _check("int8_weight_code_sums",
+           lib().int8_weight_code_sums(_ptr(CB), out, d, _ptr(sums), _stream(CB.device)))
+    return sums
+
+
+def int8_matmul_zeropoint(X, CB, SCB, CBsum, threshold: float = 6.0, bias=None, Y=None,
+                          workspace=None) -> torch.Tensor:
+    """The matmul with zeropoint activation codes: fp16 X [T, in] -> fp16 Y [T, out]."""
+    _need(X, torch.float16, "X")
+    _need(CB, torch.int8, "CB")
+    _need(SCB, torch.float32, "SCB")
+    _need(CBsum, torch.int32, "CBsum")
+    T, d = X.shape
+    out = CB.shape[0]
+    if bias is not None:
+        _need(bias, torch.float16, "bias")
+    if Y is None:
+        Y = torch.empty((T, out), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(T, d, out, X.device)
+    _check("int8_matmul_zeropoint", lib().int8_matmul_zeropoint(
+        _ptr(X), T, d, _ptr(CB), _ptr(SCB), _ptr(CBsum), out, float(threshold), _ptr(bias),
+        _ptr(Y), _ptr(workspace), workspace.numel(), _stream(X.device)))
+    return Y
+
+
+def int8_matmul_zeropoint_debug(X, CB, SCB, CBsum, threshold: float = 6.0, bias=None,
+                                workspace=None):
+    """int8_matmul_zeropoint plus its intermediates: dict of Y, idx, n_out, Xq, S, Z, acc."""
+    _need(X, torch.float16, "X")
+    T, d = X.shape
+    out = CB.shape[0]
+    dev = X.device
+    Y = torch.empty((T, out), dtype=torch.float16, device=dev)
+    idx = torch.full((d,), -1, dtype=torch.int32, device=dev)
+    n = torch.zeros(4, dtype=torch.int32, device=dev)
+    Xq = torch.empty((T, d), dtype=torch.int8, device=dev)
+    S = torch.empty(T, dtype=torch.float32, device=dev)
+    Z = torch.empty(T, dtype=torch.float32, device=dev)
+    acc = torch.empty((T, out), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(T, d, out, dev)
+    _check("int8_matmul_zeropoint_debug", lib().int8_matmul_zeropoint_debug(
+        _ptr(X), T, d, _ptr(CB), _ptr(SCB), _ptr(CBsum), out, float(threshold), _ptr(bias),
+        _ptr(Y), _ptr(workspace), workspace.numel(), _stream(dev), _ptr(idx), _ptr(n),
+        _ptr(Xq), _ptr(S), _ptr(Z), _ptr(acc)))
+    n_out = int(n[0].item())
+    return {"Y": Y, "idx": idx[:n_out], "n_out": n_out, "Xq": Xq, "S": S, "Z": Z, "acc": acc,
+            "workspace": workspace}
 
 
 def int8_ffn_workspace_size(T: int, d_model: int, d_ff: int, max_outlier_cols: int = 0) -> int:

@@ -90,6 +90,10 @@ struct Layer {
   const WsHeader* prev = nullptr;  // its status word, carried into this one
   int8_t* dbg_xq = nullptr;
   int32_t* dbg_acc = nullptr;
+  // zeropoint activation codes (tensor-core kernel at every T): the weight's code sums
+  const int32_t* zp_cbsum = nullptr;
+  float* dbg_S = nullptr;
+  float* dbg_Z = nullptr;
   uint64_t stall_ns = 0;
   int prof_base = -1;              // profiling events prof_base .. +3, or -1: none
 };
@@ -112,7 +116,8 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
   if (st != I8_OK) return st;
   ++g_last_launches;
   if (ly.prof_base >= 0) prof_mark(ly.prof_base + 1, s);
-  if (gemv_fits(ly.T, ly.in)) {
+  const bool zp = ly.zp_cbsum != nullptr;
+  if (!zp && gemv_fits(ly.T, ly.in)) {
     // decode sizes: int8 codes for the CUDA-core matmul, which reads the outlier weights
     // from CB itself (no W_out gather)
     int8_t* xq8 = reinterpret_cast<int8_t*>(ws + L.xq);
@@ -145,10 +150,18 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
                                      cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return I8_ERR_CUDA;
   } else {
-    if ((st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
-                                               mask, idx, ncap, ws + L.xq, rowabs, ws + L.xout,
-                                               ws + L.wout, l1, ly.dbg_xq, s))) != I8_OK)
-      return st;
+    int32_t* zi = reinterpret_cast<int32_t*>(ws + L.zi);
+    int32_t* cbout = reinterpret_cast<int32_t*>(ws + L.cbout);
+    if (zp)
+      st = from_cuda(launch_quantize_gather_zp(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
+                                               mask, idx, ncap, ws + L.xq, rowabs, zi,
+                                               ws + L.xout, ws + L.wout, cbout, l1, ly.dbg_xq,
+                                               ly.dbg_S, ly.dbg_Z, s));
+    else
+      st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
+                                            mask, idx, ncap, ws + L.xq, rowabs, ws + L.xout,
+                                            ws + L.wout, l1, ly.dbg_xq, s));
+    if (st != I8_OK) return st;
     ++g_last_launches;
     if (ly.prof_base >= 0) prof_mark(ly.prof_base + 2, s);
     GemmArgs g;
@@ -169,6 +182,11 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
     g.in = ly.in;
     g.out = ly.out;
     g.next = ly.next;
+    if (zp) {
+      g.zi = zi;
+      g.cbsum = ly.zp_cbsum;
+      g.cbout = cbout;
+    }
     if (ly.stall_ns) {  // test hook: nothing is loaded, so every pipeline wait runs out
       g.debug_skip_loads = 1;
       g.timeout_ns = ly.stall_ns;
@@ -184,10 +202,15 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
                      float threshold, const void* bias, void* Y, void* workspace,
                      size_t ws_bytes, void* stream, int32_t* dbg_idx, int32_t* dbg_n,
                      int8_t* dbg_xq, float* dbg_rowabs, int32_t* dbg_acc,
-                     uint64_t stall_ns = 0) {
+                     uint64_t stall_ns = 0, const int32_t* zp_cbsum = nullptr,
+                     bool zp = false, float* dbg_S = nullptr, float* dbg_Z = nullptr) {
   g_last_launches = 0;
   i8_status st = validate_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, workspace);
   if (st != I8_OK) return st;
+  if (zp && !zp_cbsum) return I8_ERR_INVALID_ARG;
+  if ((zp_cbsum && !aligned16(zp_cbsum)) || (dbg_S && !aligned16(dbg_S)) ||
+      (dbg_Z && !aligned16(dbg_Z)))
+    return I8_ERR_ALIGNMENT;
   if (stall_ns && gemv_fits(T, in)) return I8_ERR_INVALID_ARG;  // a tensor-core-path hook
   if ((dbg_idx && !aligned16(dbg_idx)) || (dbg_n && !aligned16(dbg_n)) ||
       (dbg_xq && !aligned16(dbg_xq)) || (dbg_rowabs && !aligned16(dbg_rowabs)) ||
@@ -213,6 +236,9 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   ly.dbg_xq = dbg_xq;
   ly.dbg_acc = dbg_acc;
   ly.stall_ns = stall_ns;
+  ly.zp_cbsum = zp ? zp_cbsum : nullptr;
+  ly.dbg_S = dbg_S;
+  ly.dbg_Z = dbg_Z;
   ly.prof_base = 0;
   if (cudaMemsetAsync(ly.ws, 0, ly.L.zero_bytes, s) != cudaSuccess) return I8_ERR_CUDA;
   ++g_last_launches;
@@ -385,6 +411,37 @@ I8_API i8_status i8_test_stalled_matmul(const void* X, int T, int in, const int8
   if (wait_limit_ns == 0) return I8_ERR_INVALID_ARG;
   return run_matmul(X, T, in, CB, SCB, out, 6.0f, nullptr, Y, workspace, ws_bytes, stream,
                     nullptr, nullptr, nullptr, nullptr, nullptr, wait_limit_ns);
+}
+
+I8_API i8_status int8_weight_code_sums(const int8_t* CB, int out, int in, int32_t* CBsum,
+                                       void* stream) {
+  g_last_launches = 0;
+  if (out < 0 || in < 0 || !CB || !CBsum) return I8_ERR_INVALID_ARG;
+  if (!aligned16(CB) || !aligned16(CBsum)) return I8_ERR_ALIGNMENT;
+  if (out == 0) return I8_OK;
+  i8_status st = check_device();
+  if (st != I8_OK) return st;
+  st = from_cuda(launch_code_sums(CB, out, in, CBsum, static_cast<cudaStream_t>(stream)));
+  if (st == I8_OK) g_last_launches = 1;
+  return st;
+}
+
+I8_API i8_status int8_matmul_zeropoint(const void* X, int T, int in, const int8_t* CB,
+                                       const float* SCB, const int32_t* CBsum, int out,
+                                       float threshold, const void* bias, void* Y,
+                                       void* workspace, size_t ws_bytes, void* stream) {
+  return run_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, workspace, ws_bytes, stream,
+                    nullptr, nullptr, nullptr, nullptr, nullptr, 0, CBsum, true);
+}
+
+I8_API i8_status int8_matmul_zeropoint_debug(const void* X, int T, int in, const int8_t* CB,
+                                             const float* SCB, const int32_t* CBsum, int out,
+                                             float threshold, const void* bias, void* Y,
+                                             void* workspace, size_t ws_bytes, void* stream,
+                                             int32_t* outlier_idx, int32_t* n_out, int8_t* Xq,
+                                             float* S, float* Z, int32_t* acc_s32) {
+  return run_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, workspace, ws_bytes, stream,
+                    outlier_idx, n_out, Xq, nullptr, acc_s32, 0, CBsum, true, S, Z);
 }
 
 I8_API size_t int8_ffn_workspace_size(int T, int d_model, int d_ff, int max_outlier_cols) {

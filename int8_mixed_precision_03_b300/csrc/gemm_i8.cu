@@ -32,6 +32,10 @@
 // of its tile is folded into it, and the tile's last segment reads it back.
 // Epilogue: Y[t, o] = fp16(acc * rowabs[t] * SCB[o] / 127^2 + outlier + bias[o]), staged
 // per warp in shared memory (two boxes of tokens x 32 features) and written by TMA stores.
+// With zeropoint activation codes (x ~ (q + Z)/S per token, "LLM.int8() summary" (zenn),
+// "Zeropoint Quantization") the epilogue adds Z_t times the feature's code sum over the
+// inlier columns to the exact int32 product, in 64-bit integers, before scaling by
+// rowabs = 127/S.
 // When Y is the input of a following int8 matmul (an FFN's up projection), the epilogue
 // also applies the activation (ReLU or none) and computes that matmul's outlier flags:
 // each lane owns one column of Y, keeps the largest fp16 magnitude over the tile's valid
@@ -95,12 +99,17 @@ struct Params {
   uint32_t* next_mask;        // FFN up projection: the next matmul's outlier mask
   uint32_t next_thr;          // its threshold as fp16 magnitude bits
   int next_relu;              // ReLU on Y before the statistics
+  int z_safe;                 // zeropoint: |Z| up to which acc + Z * cbin fits in int32
+  const int32_t* zi;          // zeropoint variant: per-token zero points [T]
+  const int32_t* cbsum;       // and per-feature code sums over all / outlier columns
+  const int32_t* cbout;
   uint64_t timeout_ns;
   int debug_skip_loads;
 };
 
-// Epilogue variants: plain, plain + int32 export, activation + next matmul's column flags.
-enum EpiMode { kEpiPlain = 0, kEpiDebug = 1, kEpiNext = 2 };
+// Epilogue variants: plain, plain + int32 export, activation + next matmul's column flags,
+// zeropoint codes (acc + zi[t] * inlier code sum of feature o), the same + int32 export.
+enum EpiMode { kEpiPlain = 0, kEpiDebug = 1, kEpiNext = 2, kEpiZp = 3, kEpiZpDebug = 4 };
 
 __device__ __forceinline__ int outlier_kblocks(const Params& p) {
   const int n = *reinterpret_cast<volatile const int*>(&p.hdr->n_out_used);
@@ -143,7 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmY, const Params p) {
   using C = Cfg<BN>;
   constexpr int kS = C::kStages, kS8 = C::kStages8, kW = C::kW;
-  constexpr bool kDebug = kMode == kEpiDebug, kNext = kMode == kEpiNext;
+  constexpr bool kDebug = kMode == kEpiDebug || kMode == kEpiZpDebug;
+  constexpr bool kNext = kMode == kEpiNext;
+  constexpr bool kZp = kMode == kEpiZp || kMode == kEpiZpDebug;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + C::bars);
@@ -392,11 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
       const float so = o_ok ? __ldg(&p.scb[o]) * (1.0f / 16129.0f) : 0.0f;
       float ra[kNR];  // row scales of the tile's tokens, 32 per register, one per lane
+      [[maybe_unused]] int za[kZp ? kNR : 1];  // zeropoint: the tokens' zero points
 #pragma unroll
       for (int i = 0; i < kNR; ++i) {
         const int tk = n0 + 32 * i + lane;
         ra[i] = tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f;
+        if constexpr (kZp) za[i] = tk < p.T ? __ldg(&p.zi[tk]) : 0;
       }
+      // zeropoint: sum of this feature's codes over the inlier columns
+      [[maybe_unused]] const int cbin =
+          (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
       const int nseg_int = count_int_segments(p, n_blk);
       const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
       uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
@@ -455,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (lane == 0) mbar_arrive(&tmem_empty[b]);
             }
             const float ra_s = ra[0];  // this slice's tokens, one per lane
+            [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
             uint32_t yh[kW / 2];
 #pragma unroll
             for (int j = 0; j < kW; ++j) {
@@ -467,7 +484,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
               }
               const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
-              float y = (float)acc * (rj * so) + fo + bo;
+              float y;
+              if constexpr (kZp) {
+                // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
+                // when |Z| <= z_safe bounds it below 2^31 (token j is the same for the
+                // whole warp, so the branch is uniform), in 64 bits otherwise
+                const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
+                if (abs(zj) <= p.z_safe) {
+                  y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
+                } else {
+                  const long long az = (long long)acc + (long long)zj * (long long)cbin;
+                  y = __ll2float_rn(az) * (rj * so) + fo + bo;
+                }
+              } else {
+                y = (float)acc * (rj * so) + fo + bo;
+              }
               if constexpr (kNext) {
                 if (p.next_relu) y = fmaxf(y, 0.0f);
               }
@@ -492,6 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales
 #pragma unroll
               for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
+              if constexpr (kZp) {
+#pragma unroll
+                for (int i = 0; i + 1 < kNR; ++i) za[i] = za[i + 1];
+              }
             }
           }
           if constexpr (kNext) {  // the tile's flags of columns m0 + 32q .. + 31
@@ -565,12 +600,24 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.next_mask = a.next.mask;
   p.next_thr = a.next.thr_bits;
   p.next_relu = a.next.relu;
+  // |acc| <= 127^2 in and |cbin| <= 127 in, so |acc + Z cbin| < 2^31 while
+  // |Z| <= (2^31 - 1 - 127^2 in) / (127 in)
+  p.z_safe = (int)((2147483647LL - 16129LL * a.in) / (127LL * a.in));
+  p.zi = a.zi;
+  p.cbsum = a.cbsum;
+  p.cbout = a.cbout;
   p.timeout_ns = a.timeout_ns;
   p.debug_skip_loads = a.debug_skip_loads;
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < kSmCount ? tiles : kSmCount;
   // ReLU comes only with the statistics epilogue (an FFN's up projection)
-  if ((a.next.relu && !a.next.mask) || (a.next.mask && a.acc_debug)) return cudaErrorInvalidValue;
+  if ((a.next.relu && !a.next.mask) || (a.next.mask && (a.acc_debug || a.zi)))
+    return cudaErrorInvalidValue;
+  if (a.zi && (!a.cbsum || !a.cbout)) return cudaErrorInvalidValue;
+  if (a.zi) {
+    if (a.acc_debug) return launch_kernel<BN, kEpiZpDebug>(s, mA8, mB, mWo, mXo, mY, p, grid);
+    return launch_kernel<BN, kEpiZp>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  }
   if (a.next.mask) return launch_kernel<BN, kEpiNext>(s, mA8, mB, mWo, mXo, mY, p, grid);
   if (a.acc_debug) return launch_kernel<BN, kEpiDebug>(s, mA8, mB, mWo, mXo, mY, p, grid);
   return launch_kernel<BN, kEpiPlain>(s, mA8, mB, mWo, mXo, mY, p, grid);

@@ -35,6 +35,8 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 // int8_matmul_workspace_size() and int8_matmul().
 struct WsLayout {
   size_t header = 0, mask = 0, l1 = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0;
+  size_t zi = 0;          // zeropoint variant: int32 per-row zero points [T]
+  size_t cbout = 0;       // zeropoint variant: int32 sums of the outlier columns' codes [out]
   size_t acc = 0;         // int32 running sums of the matmul's epilogue, one tile per SM
   size_t total = 0;
   size_t zero_bytes = 0;  // header + mask + l1: memset at the start of every call
@@ -61,6 +63,8 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.rowabs = off; off = align_up(off + 4 * (size_t)T, 256);
   L.xout = off; off = align_up(off + 2 * (size_t)T * ncap, 256);
   L.wout = off; off = align_up(off + 2 * (size_t)out * ncap, 256);
+  L.zi = off; off = align_up(off + 4 * (size_t)T, 256);
+  L.cbout = off; off = align_up(off + 4 * (size_t)out, 256);
   L.acc = off; off = align_up(off + 4 * (size_t)kSmCount * 128 * i8_bn(T), 256);
   L.total = off;
   return L;
@@ -91,6 +95,20 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
                                    int32_t* l1, int8_t* xq8_debug, cudaStream_t s);
+// Zeropoint variant of quantize + gather: per row S, Z over the inlier columns, codes
+// clamp(rint(x*S - Z)) (outlier columns 0) as fp16, the epilogue's row factor
+// rowabs[i] = 127/S (127*min for a constant row) and zero point zi[i] = Z (1 for a constant
+// row), X_out; per output feature W_out and cbout[o] = sum of CB over the outlier columns.
+// dbg_S, dbg_Z, xq8_debug are optional exports.
+cudaError_t launch_quantize_gather_zp(const void* X, int T, int in, const int8_t* CB,
+                                      const float* SCB, int out, const WsHeader* hdr,
+                                      const uint32_t* mask, const int32_t* idx, int ncap,
+                                      void* xq16, float* rowabs, int32_t* zi, void* xout,
+                                      void* wout, int32_t* cbout, int32_t* l1,
+                                      int8_t* xq8_debug, float* dbg_S, float* dbg_Z,
+                                      cudaStream_t s);
+// Sum of each row's int8 codes: CBsum[o] = sum_j CB[o, j] (int32).
+cudaError_t launch_code_sums(const int8_t* CB, int out, int in, int32_t* CBsum, cudaStream_t s);
 cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
                                cudaStream_t s);
 cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
@@ -117,6 +135,11 @@ struct GemmArgs {
   int32_t* acc_debug = nullptr; // optional [T, out] int32 export
   int T = 0, in = 0, out = 0;
   NextLayer next;               // int8 path: ReLU + next layer's column statistics
+  // zeropoint variant (int8 path): per-row zero points, per-feature code sums of all
+  // columns and of the outlier columns; the epilogue adds zi * (cbsum - cbout) to acc
+  const int32_t* zi = nullptr;
+  const int32_t* cbsum = nullptr;
+  const int32_t* cbout = nullptr;
   int relu = 0;                 // fp16 comparator: ReLU on Y
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)

@@ -205,6 +205,34 @@ __global__ void __launch_bounds__(kRowThreads) absmax_rows_kernel(
   if (threadIdx.x == 0) amax[row] = a;
 }
 
+// Blocks [T, ..) of the quantize passes: 32 output features per block, 8 threads per
+// feature o: W_out[o, k] = fp16((CB[o,idx[k]]*SCB[o])/127) for k < n, zeros up to npad.
+// Returns, in the feature's first thread, sum_k CB[o, idx[k]] (the other threads: partial).
+__device__ int gather_outlier_weights(const int8_t* __restrict__ CB,
+                                      const float* __restrict__ SCB, int in, int out,
+                                      const int32_t* __restrict__ idx, int n, int npad,
+                                      int ncap, int T, uint16_t* __restrict__ wout) {
+  const int o = (blockIdx.x - T) * 32 + (threadIdx.x >> 3);
+  int csum = 0;
+  if (o < out) {
+    const float scb = __ldg(&SCB[o]);
+    for (int k = threadIdx.x & 7; k < npad; k += 8) {
+      uint16_t v = 0;
+      if (k < n) {
+        const int cb = __ldg(&CB[(size_t)o * in + __ldg(&idx[k])]);
+        csum += cb;
+        v = __half_as_ushort(__float2half_rn(__fdiv_rn(__fmul_rn((float)cb, scb), 127.0f)));
+      }
+      wout[(size_t)o * ncap + k] = v;
+    }
+  }
+  // the 8 threads of a feature are 8 consecutive lanes
+  csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+  csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+  csum += __shfl_xor_sync(0xffffffffu, csum, 4);
+  return csum;
+}
+
 // Fused activation quantize + outlier gather of the matmul.
 //   blocks [0, T): row i -> fp16 codes (outlier columns 0), rowabs[i], and
 //                  X_out[i, k] = X[i, idx[k]] for k < n, zeros up to a multiple of 64;
@@ -240,17 +268,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
       xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
   } else {
     if (npad == 0) return;
-    const int o = (blockIdx.x - T) * 32 + (threadIdx.x >> 3);
-    if (o >= out) return;
-    const float scb = __ldg(&SCB[o]);
-    for (int k = threadIdx.x & 7; k < npad; k += 8) {
-      uint16_t v = 0;
-      if (k < n) {
-        const float c = (float)__ldg(&CB[(size_t)o * in + __ldg(&idx[k])]);
-        v = __half_as_ushort(__float2half_rn(__fdiv_rn(__fmul_rn(c, scb), 127.0f)));
-      }
-      wout[(size_t)o * ncap + k] = v;
-    }
+    gather_outlier_weights(CB, SCB, in, out, idx, n, npad, ncap, T, wout);
   }
 }
 
@@ -339,6 +357,209 @@ __global__ void __launch_bounds__(kRowThreads) zeropoint_rows_kernel(
   }
 }
 
+// ---------------------------------------------------------------- zeropoint variant
+// Zeropoint codes of the 8 values of chunk c (masked columns 0; all 0 when the row has no
+// spread); writes q8 / q16 (either may be null) and returns sum |code|.
+__device__ __forceinline__ int chunk_zp_codes(const uint4& v, uint32_t mb, bool spread,
+                                              float sc, float z, int c,
+                                              int8_t* __restrict__ q8,
+                                              uint16_t* __restrict__ q16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int q[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    q[2 * k] = zp_code(h2f(w[k] & 0xffffu), sc, z);
+    q[2 * k + 1] = zp_code(h2f(w[k] >> 16), sc, z);
+  }
+  int a1 = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (!spread || ((mb >> e) & 1u)) q[e] = 0;
+    a1 += abs(q[e]);
+  }
+  if (q8) {
+    uint2 o;
+    o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
+          ((uint32_t)(q[3] & 0xff) << 24);
+    o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
+          ((uint32_t)(q[7] & 0xff) << 24);
+    reinterpret_cast<uint2*>(q8)[c] = o;
+  }
+  if (q16) {
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      ow[k] = (uint32_t)__half_as_ushort(__int2half_rn(q[2 * k])) |
+              ((uint32_t)__half_as_ushort(__int2half_rn(q[2 * k + 1])) << 16);
+    reinterpret_cast<uint4*>(q16)[c] = o;
+  }
+  return a1;
+}
+
+// Min and max of the unmasked values of a chunk, folded into mn / mx.
+__device__ __forceinline__ void chunk_minmax(const uint4& v, uint32_t mb, float& mn,
+                                             float& mx) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if ((mb >> e) & 1u) continue;
+    const float x = h2f(e & 1 ? w[e >> 1] >> 16 : w[e >> 1] & 0xffffu);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+}
+
+// Block-wide min and max (kRowThreads threads).
+__device__ __forceinline__ void block_minmax(float& mn, float& mx, float* s_mn, float* s_mx) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { s_mn[warp] = mn; s_mx[warp] = mx; }
+  __syncthreads();
+  mn = s_mn[0];
+  mx = s_mx[0];
+#pragma unroll
+  for (int w = 1; w < kRowThreads / 32; ++w) { mn = fminf(mn, s_mn[w]); mx = fmaxf(mx, s_mx[w]); }
+  __syncthreads();
+}
+
+// Zeropoint quantization of one row over its unmasked columns, the analogue of
+// quantize_row (same kNV register staging, same per-chunk code statistics in s_l1):
+// S = 254/(max - min), Z = rint(S*min) + 127, code = clamp(rint(x*S - Z)); no unmasked
+// column gives min = max = 0; no spread gives S = 0, Z = min and codes 0.
+template <int kNV>
+__device__ void quantize_row_zp(const uint16_t* __restrict__ x, int cols, const uint32_t* smask,
+                                int8_t* __restrict__ q8, uint16_t* __restrict__ q16,
+                                float* s_mn, float* s_mx, int* s_l1, float& S, float& Z) {
+  const int tid = threadIdx.x;
+  const bool vec = (cols & 7) == 0;
+  const int nch = cols >> 3;
+  float mn = INFINITY, mx = -INFINITY;
+  [[maybe_unused]] uint4 v[kNV > 0 ? kNV : 1];
+  if constexpr (kNV > 0) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      v[i] = c < nch ? __ldg(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0, 0, 0, 0);
+      if (c < nch) chunk_minmax(v[i], chunk_mask(smask, c), mn, mx);
+    }
+  } else if (vec) {
+    for (int c = tid; c < nch; c += kRowThreads)
+      chunk_minmax(__ldg(reinterpret_cast<const uint4*>(x) + c), chunk_mask(smask, c), mn, mx);
+  } else {
+    for (int j = tid; j < cols; j += kRowThreads) {
+      if (is_masked(smask, j)) continue;
+      const float xv = h2f(x[j]);
+      mn = fminf(mn, xv);
+      mx = fmaxf(mx, xv);
+    }
+  }
+  block_minmax(mn, mx, s_mn, s_mx);
+  if (!(mn <= mx)) { mn = 0.0f; mx = 0.0f; }  // no unmasked column
+  const bool spread = mx > mn;
+  const float sc = spread ? __fdiv_rn(254.0f, __fsub_rn(mx, mn)) : 0.0f;
+  const float z = spread ? __fadd_rn(rintf(__fmul_rn(sc, mn)), 127.0f) : mn;
+  S = sc;
+  Z = z;
+  if constexpr (kNV > 0) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int c = tid + i * kRowThreads;
+      int a1 = c < nch ? chunk_zp_codes(v[i], chunk_mask(smask, c), spread, sc, z, c, q8, q16)
+                       : 0;
+      // the warp's 32 chunks (256 columns) lie in one 1024-column chunk
+      a1 = __reduce_add_sync(0xffffffffu, a1);
+      if ((tid & 31) == 0 && a1 > 0) atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
+    }
+  } else if (vec) {
+    for (int c = tid; c < nch; c += kRowThreads) {
+      const int a1 = chunk_zp_codes(__ldg(reinterpret_cast<const uint4*>(x) + c),
+                                    chunk_mask(smask, c), spread, sc, z, c, q8, q16);
+      if (a1 > 0) atomicAdd(&s_l1[(c * 8) / kChunkK], a1);
+    }
+  } else {
+    for (int j = tid; j < cols; j += kRowThreads) {
+      int q = spread ? zp_code(h2f(x[j]), sc, z) : 0;
+      if (is_masked(smask, j)) q = 0;
+      if (q8) q8[j] = (int8_t)q;
+      if (q16) q16[j] = __half_as_ushort(__int2half_rn(q));
+      if (q) atomicAdd(&s_l1[j / kChunkK], abs(q));
+    }
+  }
+}
+
+// The zeropoint variant of quantize_gather_kernel (see launch_quantize_gather_zp).
+template <int kNV>
+__global__ void __launch_bounds__(kRowThreads) quantize_gather_zp_kernel(
+    const uint16_t* __restrict__ X, int T, int in, const int8_t* __restrict__ CB,
+    const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
+    const uint32_t* __restrict__ mask, const int32_t* __restrict__ idx, int ncap,
+    uint16_t* __restrict__ xq16, float* __restrict__ rowabs, int32_t* __restrict__ zi,
+    uint16_t* __restrict__ xout, uint16_t* __restrict__ wout, int32_t* __restrict__ cbout,
+    int32_t* __restrict__ l1, int bn, int8_t* __restrict__ xq8, float* __restrict__ dbg_S,
+    float* __restrict__ dbg_Z) {
+  extern __shared__ uint32_t s_mask[];  // (in + 31) / 32 words
+  __shared__ float s_mn[kRowThreads / 32], s_mx[kRowThreads / 32];
+  __shared__ int s_l1[I8_MAX_IN / kChunkK];
+  const int n = hdr->n_out_used;
+  const int npad = (n + 63) / 64 * 64;
+  if (blockIdx.x < (unsigned)T) {
+    const int words = (in + 31) / 32;
+    const int nch = (in + kChunkK - 1) / kChunkK;
+    for (int w = threadIdx.x; w < words; w += kRowThreads) s_mask[w] = __ldg(&mask[w]);
+    for (int c = threadIdx.x; c < nch; c += kRowThreads) s_l1[c] = 0;
+    __syncthreads();
+    const size_t i = blockIdx.x;
+    const uint16_t* x = X + i * in;
+    float S, Z;
+    quantize_row_zp<kNV>(x, in, s_mask, xq8 ? xq8 + i * in : nullptr,
+                         xq16 ? xq16 + i * in : nullptr, s_mn, s_mx, s_l1, S, Z);
+    if (threadIdx.x == 0) {
+      // epilogue factors: y = (acc + zi * sum of inlier codes) * rowabs * SCB / 127^2
+      const bool spread = S > 0.0f;
+      rowabs[i] = spread ? __fdiv_rn(127.0f, S) : __fmul_rn(127.0f, Z);
+      zi[i] = spread ? (int32_t)Z : 1;
+      if (dbg_S) dbg_S[i] = S;
+      if (dbg_Z) dbg_Z[i] = Z;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < nch; c += kRowThreads)
+      if (s_l1[c] > 0) atomicMax(&l1[(size_t)(i / bn) * nch + c], s_l1[c]);
+    for (int k = threadIdx.x; k < npad; k += kRowThreads)
+      xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
+  } else {
+    const int csum = gather_outlier_weights(CB, SCB, in, out, idx, n, npad, ncap, T, wout);
+    const int o = (blockIdx.x - T) * 32 + (threadIdx.x >> 3);
+    if ((threadIdx.x & 7) == 0 && o < out) cbout[o] = csum;
+  }
+}
+
+// Row sums of int8 codes: one warp per row, 16-byte loads where the row allows.
+__global__ void __launch_bounds__(256) code_sums_kernel(const int8_t* __restrict__ CB, int out,
+                                                        int in, int32_t* __restrict__ sums) {
+  const int o = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (o >= out) return;
+  const int8_t* row = CB + (size_t)o * in;
+  int acc = 0;
+  if (in % 16 == 0) {
+    for (int c = lane; c < in / 16; c += 32) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+      acc = __dp4a((int)v.x, 0x01010101, acc);
+      acc = __dp4a((int)v.y, 0x01010101, acc);
+      acc = __dp4a((int)v.z, 0x01010101, acc);
+      acc = __dp4a((int)v.w, 0x01010101, acc);
+    }
+  } else {
+    for (int j = lane; j < in; j += 32) acc += row[j];
+  }
+  acc = __reduce_add_sync(0xffffffffu, acc);
+  if (lane == 0) sums[o] = acc;
+}
+
 // Instantiates F<kNV> for the register depth that fits `cols` (0: two-pass path).
 #define I8_DISPATCH_NV(cols, F)                      \
   switch (row_nv(cols)) {                            \
@@ -385,6 +606,31 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
       static_cast<uint16_t*>(wout), l1, i8_bn(T), xq8_debug)
   I8_DISPATCH_NV(in, I8_LAUNCH)
 #undef I8_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_gather_zp(const void* X, int T, int in, const int8_t* CB,
+                                      const float* SCB, int out, const WsHeader* hdr,
+                                      const uint32_t* mask, const int32_t* idx, int ncap,
+                                      void* xq16, float* rowabs, int32_t* zi, void* xout,
+                                      void* wout, int32_t* cbout, int32_t* l1,
+                                      int8_t* xq8_debug, float* dbg_S, float* dbg_Z,
+                                      cudaStream_t s) {
+  const int wblocks = (out + 31) / 32;
+  const size_t smem = sizeof(uint32_t) * (size_t)((in + 31) / 32);
+#define I8_LAUNCH(NV)                                                                       \
+  quantize_gather_zp_kernel<NV><<<T + wblocks, kRowThreads, smem, s>>>(                      \
+      static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,           \
+      static_cast<uint16_t*>(xq16), rowabs, zi, static_cast<uint16_t*>(xout),               \
+      static_cast<uint16_t*>(wout), cbout, l1, i8_bn(T), xq8_debug, dbg_S, dbg_Z)
+  I8_DISPATCH_NV(in, I8_LAUNCH)
+#undef I8_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_code_sums(const int8_t* CB, int out, int in, int32_t* CBsum,
+                             cudaStream_t s) {
+  code_sums_kernel<<<(out + 7) / 8, 256, 0, s>>>(CB, out, in, CBsum);
   return cudaGetLastError();
 }
 

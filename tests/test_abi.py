@@ -171,3 +171,18 @@ def test_f16_ffn_validation(L):
     assert L.f16_ffn(p, 4, 32, 40, p, None, p, None, 1, p, p, None) == 2
     assert L.f16_ffn(p, 4, 32, 64, p, None, p, None, 1, p, None, None) == 1
     assert L.f16_ffn(p, 0, 32, 64, p, None, p, None, 1, p, p, None) == 0
+
+
+def test_zeropoint_entry_points_validate(L):
+    p = fake(A)
+    need = L.int8_matmul_workspace_size(16, 256, 1024, 0)
+    # CBsum missing, misaligned; T == 0 is a no-op
+    assert L.int8_matmul_zeropoint(p, 16, 256, p, p, None, 1024, 6.0, None, p, p, need,
+                                   None) == 1
+    assert L.int8_matmul_zeropoint(p, 16, 256, p, p, fake(A + 4), 1024, 6.0, None, p, p, need,
+                                   None) == 2
+    assert L.int8_matmul_zeropoint(p, 0, 256, p, p, p, 1024, 6.0, None, p, p, need, None) == 0
+    assert L.int8_weight_code_sums(None, 4, 16, p, None) == 1
+    assert L.int8_weight_code_sums(p, 4, 16, fake(A + 2), None) == 2
+    assert L.int8_weight_code_sums(p, 0, 16, p, None) == 0
+    assert L.i8_last_launch_count() == 0
