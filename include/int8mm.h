@@ -73,7 +73,11 @@ i8_status int8_quantize_weight(const void* W, int out, int in, int8_t* CB, float
 /*
  * Bytes of device workspace int8_matmul needs for these sizes. max_outlier_cols is the
  * largest number of outlier columns the call must handle (<= 0 means `in`, the worst
- * case); it is rounded up to a multiple of 64. Returns 0 for invalid sizes.
+ * case); it is rounded up to a multiple of 64. Returns 0 for invalid sizes. The size
+ * includes the slots of the split schedule, used when whole tiles per CTA would leave
+ * the last wave of the tensor-core matmul unbalanced (tiles are then cut between CTAs
+ * by 1024-K chunks); a workspace too small for them runs the unsplit schedule, which
+ * needs less.
  */
 size_t int8_matmul_workspace_size(int T, int in, int out, int max_outlier_cols);
 

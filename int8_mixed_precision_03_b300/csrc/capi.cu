@@ -49,11 +49,11 @@ i8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? I8_OK : I8_ERR_CU
 int ncap_limit(int in) { return (int)align_up((size_t)in, 64); }
 
 // Largest outlier capacity (multiple of 64, at most ceil64(in)) whose layout fits.
-int ncap_for_bytes(int T, int in, int out, size_t ws_bytes) {
+int ncap_for_bytes(int T, int in, int out, size_t ws_bytes, bool split_ok) {
   int hi = ncap_limit(in) / 64, lo = 0;
   while (lo < hi) {  // largest k in [0, hi] with layout(64k) fitting
     const int mid = (lo + hi + 1) / 2;
-    if (ws_layout(T, in, out, 64 * mid).total <= ws_bytes) lo = mid; else hi = mid - 1;
+    if (ws_layout(T, in, out, 64 * mid, split_ok).total <= ws_bytes) lo = mid; else hi = mid - 1;
   }
   return 64 * lo;
 }
@@ -182,6 +182,12 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
     g.in = ly.in;
     g.out = ly.out;
     g.next = ly.next;
+    if (L.split) {
+      g.split = L.split;
+      g.part = reinterpret_cast<int32_t*>(ws + L.part);
+      g.part_f = reinterpret_cast<float*>(ws + L.part_f);
+      g.tile_cnt = reinterpret_cast<int32_t*>(ws + L.tile_cnt);
+    }
     if (zp) {
       g.zi = zi;
       g.cbsum = ly.zp_cbsum;
@@ -217,7 +223,13 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
       (dbg_acc && !aligned16(dbg_acc)))
     return I8_ERR_ALIGNMENT;
   if (T == 0 || out == 0) return I8_OK;
-  const int ncap = ncap_for_bytes(T, in, out, ws_bytes);
+  // the split schedule's slots if the workspace holds them, else the unsplit schedule
+  bool split_ok = true;
+  int ncap = ncap_for_bytes(T, in, out, ws_bytes, true);
+  if (ncap < 64) {
+    split_ok = false;
+    ncap = ncap_for_bytes(T, in, out, ws_bytes, false);
+  }
   if (ncap < 64) return I8_ERR_WORKSPACE;
   if ((st = check_device()) != I8_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -232,7 +244,7 @@ i8_status run_matmul(const void* X, int T, int in, const int8_t* CB, const float
   ly.bias = bias;
   ly.Y = Y;
   ly.ws = static_cast<uint8_t*>(workspace);
-  ly.L = ws_layout(T, in, out, ncap);
+  ly.L = ws_layout(T, in, out, ncap, split_ok);
   ly.dbg_xq = dbg_xq;
   ly.dbg_acc = dbg_acc;
   ly.stall_ns = stall_ns;
@@ -266,23 +278,24 @@ struct FfnPlan {
   size_t up_off = 0, total = 0;
 };
 
-FfnPlan ffn_plan(int T, int d_model, int d_ff, int cap) {
+FfnPlan ffn_plan(int T, int d_model, int d_ff, int cap, bool split_ok = true) {
   FfnPlan P;
   const int cap_up = std::min(cap, ncap_limit(d_model));
   const int cap_down = std::min(cap, ncap_limit(d_ff));
-  P.down = ws_layout(T, d_ff, d_model, cap_down);
-  P.up = ws_layout(T, d_model, d_ff, cap_up);
+  P.down = ws_layout(T, d_ff, d_model, cap_down, split_ok);
+  P.up = ws_layout(T, d_model, d_ff, cap_up, split_ok);
   P.up_off = align_up(P.down.total, 256);
   P.total = P.up_off + P.up.total;
   return P;
 }
 
 // Largest capacity (multiple of 64, at most the wider input's limit) whose plan fits.
-int ffn_cap_for_bytes(int T, int d_model, int d_ff, size_t ws_bytes) {
+int ffn_cap_for_bytes(int T, int d_model, int d_ff, size_t ws_bytes, bool split_ok) {
   int hi = std::max(ncap_limit(d_model), ncap_limit(d_ff)) / 64, lo = 0;
   while (lo < hi) {
     const int mid = (lo + hi + 1) / 2;
-    if (ffn_plan(T, d_model, d_ff, 64 * mid).total <= ws_bytes) lo = mid; else hi = mid - 1;
+    if (ffn_plan(T, d_model, d_ff, 64 * mid, split_ok).total <= ws_bytes) lo = mid;
+    else hi = mid - 1;
   }
   return 64 * lo;
 }
@@ -305,11 +318,16 @@ i8_status run_ffn(const void* X, int T, int d_model, int d_ff, const int8_t* CB_
       (dbg_n && !aligned16(dbg_n)))
     return I8_ERR_ALIGNMENT;
   if (T == 0) return I8_OK;
-  const int cap = ffn_cap_for_bytes(T, d_model, d_ff, ws_bytes);
+  bool split_ok = true;
+  int cap = ffn_cap_for_bytes(T, d_model, d_ff, ws_bytes, true);
+  if (cap < 64) {
+    split_ok = false;
+    cap = ffn_cap_for_bytes(T, d_model, d_ff, ws_bytes, false);
+  }
   if (cap < 64) return I8_ERR_WORKSPACE;
   if ((st = check_device()) != I8_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const FfnPlan P = ffn_plan(T, d_model, d_ff, cap);
+  const FfnPlan P = ffn_plan(T, d_model, d_ff, cap, split_ok);
   uint8_t* ws_down = static_cast<uint8_t*>(workspace);
   uint8_t* ws_up = ws_down + P.up_off;
   const uint16_t thr_bits = threshold_to_half_bits(threshold);

@@ -75,8 +75,8 @@ struct Cfg {
   static constexpr int box = a8 + kStages8 * kA8Bytes;
   static constexpr int bars = box + 4 * 2 * kBoxBytes;
   // full_a, full_b, empty [kStages]; a8_full, a8_empty [kStages8]; tmem_full,
-  // tmem_empty [2]; done
-  static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * 2 + 1;
+  // tmem_empty [2]; done; epi (the four epilogue warps' rendezvous of split tiles)
+  static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * 2 + 2;
   static constexpr int misc = bars + kNumBars * 8;
   static constexpr int total = misc + 16 + 1024;  // + alignment slack
   static_assert(b % 1024 == 0 && kBBytes % 1024 == 0 && a8 % 1024 == 0, "alignment");
@@ -103,9 +103,58 @@ struct Params {
   const int32_t* zi;          // zeropoint variant: per-token zero points [T]
   const int32_t* cbsum;       // and per-feature code sums over all / outlier columns
   const int32_t* cbout;
+  // split schedule (split != 0): units are (tile, 1024-K chunk) in tile-major order and
+  // CTA b takes units [units*b/G, units*(b+1)/G); tiles cut between CTAs finish through
+  // the part slots and a per-tile arrival counter (the last piece to arrive writes Y)
+  int split;
+  long long units;
+  int32_t* part;              // [G][2][BN][128] int32: a CTA's first / last piece's sums
+  float* part_f;              // [G][BN][128] fp32: outlier sums of a tile-ending piece
+  int32_t* tile_cnt;          // [tiles] arrivals, zeroed per call
   uint64_t timeout_ns;
   int debug_skip_loads;
 };
+
+// The pieces of work of one CTA: whole tiles t = b, b + G, ... (unsplit), or the runs of
+// its unit range that fall in one tile (split). A piece is (tile t, chunks [c0, c1)); its K
+// blocks are [16 c0, min(16 c1, nkb)) plus the outlier K blocks when c1 == nchunks.
+template <bool kSplit>
+struct Sched {
+  long long u = 0, ue = 0;
+  int t = 0;
+  __device__ explicit Sched(const Params& p) {
+    if constexpr (kSplit) {
+      u = p.units * blockIdx.x / gridDim.x;
+      ue = p.units * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      t = blockIdx.x;
+    }
+  }
+  __device__ bool next(const Params& p, int& tt, int& c0, int& c1) {
+    if constexpr (!kSplit) {
+      if (t >= p.m_tiles * p.n_tiles) return false;
+      tt = t;
+      c0 = 0;
+      c1 = p.nchunks;
+      t += gridDim.x;
+      return true;
+    }
+    if (u >= ue) return false;
+    tt = (int)(u / p.nchunks);
+    c0 = (int)(u % p.nchunks);
+    const long long e = min(ue, (long long)(tt + 1) * p.nchunks);
+    c1 = c0 + (int)(e - u);
+    u = e;
+    return true;
+  }
+};
+// First unit of CTA b, and the CTA that owns unit u, under the split schedule.
+__device__ __forceinline__ long long unit_start(const Params& p, int b) {
+  return p.units * b / gridDim.x;
+}
+__device__ __forceinline__ int unit_owner(const Params& p, long long u) {
+  return (int)(((u + 1) * gridDim.x + p.units - 1) / p.units - 1);
+}
 
 // Epilogue variants: plain, plain + int32 export, activation + next matmul's column flags,
 // zeropoint codes (acc + zi[t] * inlier code sum of feature o), the same + int32 export.
@@ -122,19 +171,19 @@ __device__ __forceinline__ uint32_t chunk_bound(const Params& p, int n_blk, int 
   return 127u * (uint32_t)__ldg(&p.l1[(size_t)n_blk * p.nchunks + c]);
 }
 // Greedy rule shared by the MMA issuer and the epilogue: chunk c opens a new segment when
-// it is the first chunk or adding its bound would exceed 2^24.
+// it is the first chunk of a piece or adding its bound would exceed 2^24.
 struct SegWalker {
   uint32_t run = 0;
-  __device__ __forceinline__ bool opens(uint32_t b, int c) {
-    if (c == 0 || run + b > kExactLimit) { run = b; return true; }
+  __device__ __forceinline__ bool opens(uint32_t b, bool first) {
+    if (first || run + b > kExactLimit) { run = b; return true; }
     run += b;
     return false;
   }
 };
-__device__ __forceinline__ int count_int_segments(const Params& p, int n_blk) {
+__device__ __forceinline__ int count_int_segments(const Params& p, int n_blk, int c0, int c1) {
   SegWalker w;
   int n = 0;
-  for (int c = 0; c < p.nchunks; ++c) n += w.opens(chunk_bound(p, n_blk, c), c) ? 1 : 0;
+  for (int c = c0; c < c1; ++c) n += w.opens(chunk_bound(p, n_blk, c), c == c0) ? 1 : 0;
   return n;
 }
 
@@ -145,7 +194,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, int kMode>
+template <int BN, int kMode, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmWo, const __grid_constant__ CUtensorMap tmXo,
@@ -165,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = a8_empty + kS8;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* done = tmem_empty + 2;
+  uint64_t* epi_bar = done + 1;
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::misc);
   const Abort ab{reinterpret_cast<volatile int*>(smem + C::misc + 4), p.hdr, p.timeout_ns};
 
@@ -184,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[s], 4);  // one arrival per epilogue warp
     }
     mbar_init(done, 1);
+    mbar_init(epi_bar, 4);
     *ab.flag = 0;
     fence_mbar_init();
   }
@@ -215,9 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !p.debug_skip_loads) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      Sched<kSplit> sc(p);
+      int t, c0, c1;
+      while (ok && sc.next(p, t, c0, c1)) {
         const int n0 = (t % p.n_tiles) * BN;
-        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
+        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb, ++it) {
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
           if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
           mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
@@ -239,9 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !p.debug_skip_loads) {
       uint32_t i8 = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      Sched<kSplit> sc(p);
+      int t, c0, c1;
+      while (ok && sc.next(p, t, c0, c1)) {
         const int m0 = (t / p.n_tiles) * BM;
-        for (int kb = 0; kb < nkb_all && ok; ++kb) {
+        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
+        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb) {
           const int nbox = kb < p.nkb ? 1 : 2;
           for (int h = 0; h < nbox && ok; ++h, ++i8) {
             const uint32_t s8 = i8 % kS8, ph8 = (i8 / kS8) & 1u;
@@ -266,26 +323,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_f16_f32acc(BM, BN);
       uint32_t it = 0, nseg = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      Sched<kSplit> sc(p);
+      int t, c0, c1;
+      while (ok && sc.next(p, t, c0, c1)) {
         const int n_blk = t % p.n_tiles;
         SegWalker walker;
         bool seg_first = true;
         uint32_t dcol = 0;
-        int c = -1;  // current int chunk
-        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+        int c = c0 - 1;  // current int chunk
+        const int kb_lo = c0 * kChunkKBlocks;
+        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
+        for (int kb = kb_lo; kb < kb_end && ok; ++kb, ++it) {
           // segment boundaries: int chunks grouped by the exactness bound, then the
           // outlier segment; each segment takes the next accumulator (F0/F1)
           bool opens = false;
           if (kb < p.nkb) {
             if (kb % kChunkKBlocks == 0) {
               ++c;
-              opens = walker.opens(chunk_bound(p, n_blk, c), c);
+              opens = walker.opens(chunk_bound(p, n_blk, c), c == c0);
             }
           } else {
             opens = kb == p.nkb;
           }
           if (opens) {
-            if (kb > 0) { mma_commit(&tmem_full[nseg & 1u]); ++nseg; }
+            if (kb > kb_lo) { mma_commit(&tmem_full[nseg & 1u]); ++nseg; }
             if (!(ok = pipe_wait(&tmem_empty[nseg & 1u], ((nseg >> 1) & 1u) ^ 1u, ab))) break;
             tc_fence_after();
             dcol = (nseg & 1u) * BN;
@@ -326,8 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t swz16 = (uint32_t)r & 7u;
       uint32_t it = 0, i8 = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < nkb_all && ok; ++kb, ++it) {
+      Sched<kSplit> sc(p);
+      int t, c0, c1;
+      while (ok && sc.next(p, t, c0, c1)) {
+        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
+        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb, ++it) {
           const bool is_int = kb < p.nkb;
           const uint32_t i8_0 = i8;
           i8 += is_int ? 1u : 2u;
@@ -386,80 +450,288 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
     // -------------------------------------------------------- epilogue
-    constexpr int kNR = (BN + 31) / 32;  // prefetched row scales per lane
-    const int q = warp & 3;
-    const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
-    uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
-    const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
-    // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
-    int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
-    uint32_t nseg = 0, slot = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
-      const int m0 = m_blk * BM, n0 = n_blk * BN;
-      const int o = m0 + q * 32 + lane;
-      const bool o_ok = o < p.out;
-      const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
-      const float so = o_ok ? __ldg(&p.scb[o]) * (1.0f / 16129.0f) : 0.0f;
-      float ra[kNR];  // row scales of the tile's tokens, 32 per register, one per lane
-      [[maybe_unused]] int za[kZp ? kNR : 1];  // zeropoint: the tokens' zero points
-#pragma unroll
-      for (int i = 0; i < kNR; ++i) {
-        const int tk = n0 + 32 * i + lane;
-        ra[i] = tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f;
-        if constexpr (kZp) za[i] = tk < p.T ? __ldg(&p.zi[tk]) : 0;
-      }
-      // zeropoint: sum of this feature's codes over the inlier columns
-      [[maybe_unused]] const int cbin =
-          (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
-      const int nseg_int = count_int_segments(p, n_blk);
-      const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
-      uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
-      for (int si = 0; si < nseg_tile && ok; ++si, ++nseg) {
-        const bool is_out = si >= nseg_int;
-        const bool first = si == 0;
-        const bool last = si == nseg_tile - 1;
-        const uint32_t b = nseg & 1u;
-        if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
-        tc_fence_after();
-        const uint32_t tF = tq + b * BN;
-        // Running sums of the tile (not for its first segment): slice j0's are in pc while
-        // the next slice's load into pn, so the L2 latency is paid once per segment.
-        int pn[kW];
-#pragma unroll
-        for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
-        if (!last) {
-          // an int segment that is not the last one of the tile: fold it into the
-          // running sum (first segment: store it)
-#pragma unroll 1
-          for (int j0 = 0; j0 < BN; j0 += kW) {
-            int pc[kW];
-#pragma unroll
-            for (int j = 0; j < kW; ++j) pc[j] = pn[j];
-            if (!first && j0 + kW < BN) {
-#pragma unroll
-              for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
+    if constexpr (!kSplit) {
+      // whole tiles, t = b, b + G, ...
+      constexpr int kNR = (BN + 31) / 32;  // prefetched row scales per lane
+      const int q = warp & 3;
+      const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+      uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
+      const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+      // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
+      int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
+      uint32_t nseg = 0, slot = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
+        const int m0 = m_blk * BM, n0 = n_blk * BN;
+        const int o = m0 + q * 32 + lane;
+        const bool o_ok = o < p.out;
+        const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
+        const float so = o_ok ? __ldg(&p.scb[o]) * (1.0f / 16129.0f) : 0.0f;
+        float ra[kNR];  // row scales of the tile's tokens, 32 per register, one per lane
+        [[maybe_unused]] int za[kZp ? kNR : 1] = {};  // zeropoint: the tokens' zero points
+  #pragma unroll
+        for (int i = 0; i < kNR; ++i) {
+          const int tk = n0 + 32 * i + lane;
+          ra[i] = tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f;
+          if constexpr (kZp) za[i] = tk < p.T ? __ldg(&p.zi[tk]) : 0;
+        }
+        // zeropoint: sum of this feature's codes over the inlier columns
+        [[maybe_unused]] const int cbin =
+            (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
+        const int nseg_int = count_int_segments(p, n_blk, 0, p.nchunks);
+        const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
+        uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
+        for (int si = 0; si < nseg_tile && ok; ++si, ++nseg) {
+          const bool is_out = si >= nseg_int;
+          const bool first = si == 0;
+          const bool last = si == nseg_tile - 1;
+          const uint32_t b = nseg & 1u;
+          if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
+          tc_fence_after();
+          const uint32_t tF = tq + b * BN;
+          // Running sums of the tile (not for its first segment): slice j0's are in pc while
+          // the next slice's load into pn, so the L2 latency is paid once per segment.
+          int pn[kW];
+  #pragma unroll
+          for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
+          if (!last) {
+            // an int segment that is not the last one of the tile: fold it into the
+            // running sum (first segment: store it)
+  #pragma unroll 1
+            for (int j0 = 0; j0 < BN; j0 += kW) {
+              int pc[kW];
+  #pragma unroll
+              for (int j = 0; j < kW; ++j) pc[j] = pn[j];
+              if (!first && j0 + kW < BN) {
+  #pragma unroll
+                for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
+              }
+              uint32_t f[kW];
+              tmem_ld<kW>(tF + j0, f);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int j = 0; j < kW; ++j)
+                accs[(size_t)(j0 + j) * 128] = pc[j] + __float2int_rn(__uint_as_float(f[j]));
             }
-            uint32_t f[kW];
-            tmem_ld<kW>(tF + j0, f);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < kW; ++j)
-              accs[(size_t)(j0 + j) * 128] = pc[j] + __float2int_rn(__uint_as_float(f[j]));
+            // the accumulator is free as soon as it has been read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[b]);
+          } else {
+  #pragma unroll 1
+            for (int j0 = 0; j0 < BN; j0 += kW) {
+              int pc[kW];
+  #pragma unroll
+              for (int j = 0; j < kW; ++j) pc[j] = pn[j];
+              if (!first && j0 + kW < BN) {
+  #pragma unroll
+                for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
+              }
+              uint32_t f[kW];
+              tmem_ld<kW>(tF + j0, f);
+              tmem_ld_wait();
+              if (j0 + kW >= BN) {  // all of F has been read: release it to the MMA
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty[b]);
+              }
+              const float ra_s = ra[0];  // this slice's tokens, one per lane
+              [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
+              uint32_t yh[kW / 2];
+  #pragma unroll
+              for (int j = 0; j < kW; ++j) {
+                int acc;
+                float fo = 0.0f;
+                if (is_out) {
+                  acc = pc[j];
+                  fo = __uint_as_float(f[j]);
+                } else {
+                  acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
+                }
+                const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+                float y;
+                if constexpr (kZp) {
+                  // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
+                  // when |Z| <= z_safe bounds it below 2^31 (token j is the same for the
+                  // whole warp, so the branch is uniform), in 64 bits otherwise
+                  const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
+                  if (abs(zj) <= p.z_safe) {
+                    y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
+                  } else {
+                    const long long az = (long long)acc + (long long)zj * (long long)cbin;
+                    y = __ll2float_rn(az) * (rj * so) + fo + bo;
+                  }
+                } else {
+                  y = (float)acc * (rj * so) + fo + bo;
+                }
+                if constexpr (kNext) {
+                  if (p.next_relu) y = fmaxf(y, 0.0f);
+                }
+                const uint32_t h = __half_as_ushort(__float2half_rn(y));
+                if constexpr (kNext) {
+                  if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
+                }
+                yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
+                if constexpr (kDebug) pc[j] = acc;
+              }
+              box_reuse_wait(lane);
+              box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
+                            n0 + j0, lane);
+              slot ^= 1u;
+              if constexpr (kDebug) {
+  #pragma unroll 1
+                for (int j = 0; j < kW; ++j) {
+                  const int tok = n0 + j0 + j;
+                  if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = pc[j];
+                }
+              }
+              if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales
+  #pragma unroll
+                for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
+                if constexpr (kZp) {
+  #pragma unroll
+                  for (int i = 0; i + 1 < kNR; ++i) za[i] = za[i + 1];
+                }
+              }
+            }
+            if constexpr (kNext) {  // the tile's flags of columns m0 + 32q .. + 31
+              const uint32_t word = __ballot_sync(0xffffffffu, o_ok && ymax >= p.next_thr);
+              if (lane == 0 && word != 0u) atomicOr(&p.next_mask[(m0 + 32 * q) >> 5], word);
+            }
           }
-          // the accumulator is free as soon as it has been read
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tmem_empty[b]);
-        } else {
-#pragma unroll 1
+        }
+      }
+      if (lane == 0) bulk_wait_group0();  // output stores complete before the CTA exits
+    } else {
+      // pieces of the split schedule
+      constexpr int kNR = (BN + 31) / 32;  // prefetched row scales per lane
+      const int q = warp & 3;
+      const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+      uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
+      const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+      volatile int* s_fin = reinterpret_cast<volatile int*>(smem + C::misc + 8);
+      // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
+      int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
+      uint32_t nseg = 0, slot = 0, ephase = 0;
+      bool ok = true;
+      // rendezvous of the four epilogue warps (bounded: an aborted pipeline unwinds)
+      auto epi_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_bar);
+        const bool r = pipe_wait(epi_bar, ephase & 1u, ab);
+        ++ephase;
+        return r;
+      };
+      Sched<kSplit> sc(p);
+      int t, c0, c1;
+      while (ok && sc.next(p, t, c0, c1)) {
+        const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
+        const int m0 = m_blk * BM, n0 = n_blk * BN;
+        const int o = m0 + q * 32 + lane;
+        const bool o_ok = o < p.out;
+        const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
+        const float so = o_ok ? __ldg(&p.scb[o]) * (1.0f / 16129.0f) : 0.0f;
+        float ra[kNR];  // row scales of the tile's tokens, 32 per register, one per lane
+        [[maybe_unused]] int za[kZp ? kNR : 1] = {};  // zeropoint: the tokens' zero points
+  #pragma unroll
+        for (int i = 0; i < kNR; ++i) {
+          const int tk = n0 + 32 * i + lane;
+          ra[i] = tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f;
+          if constexpr (kZp) za[i] = tk < p.T ? __ldg(&p.zi[tk]) : 0;
+        }
+        // zeropoint: sum of this feature's codes over the inlier columns
+        [[maybe_unused]] const int cbin =
+            (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
+        const bool has_out = c1 == p.nchunks && nkb_out > 0;
+        const int nseg_int = count_int_segments(p, n_blk, c0, c1);
+        const int nseg_tile = nseg_int + (has_out ? 1 : 0);
+        // a piece that is not the whole tile publishes its sums; the tile's last piece to
+        // arrive adds all pieces and writes Y
+        const bool whole = c0 == 0 && c1 == p.nchunks;
+        int32_t* my_part = nullptr;
+        float* my_part_f = nullptr;
+        if (!whole) {
+          const int pslot = unit_start(p, blockIdx.x) >= (long long)t * p.nchunks ? 0 : 1;
+          my_part = p.part + ((size_t)blockIdx.x * 2 + pslot) * BN * 128 + 32 * q + lane;
+          my_part_f = p.part_f + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
+        }
+        uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
+
+        // Y of token slice j0 from its int sums and fp32 outlier sums (one per lane = feature)
+        auto emit = [&](int j0, const int (&accv)[kW], const float (&fov)[kW]) {
+          const float ra_s = ra[0];  // this slice's tokens, one per lane
+          [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
+          uint32_t yh[kW / 2];
+  #pragma unroll
+          for (int j = 0; j < kW; ++j) {
+            const int acc = accv[j];
+            const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+            float y;
+            if constexpr (kZp) {
+              // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32 when
+              // |Z| <= z_safe bounds it below 2^31 (token j is the same for the whole warp,
+              // so the branch is uniform), in 64 bits otherwise
+              const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
+              if (abs(zj) <= p.z_safe) {
+                y = (float)(acc + zj * cbin) * (rj * so) + fov[j] + bo;
+              } else {
+                const long long az = (long long)acc + (long long)zj * (long long)cbin;
+                y = __ll2float_rn(az) * (rj * so) + fov[j] + bo;
+              }
+            } else {
+              y = (float)acc * (rj * so) + fov[j] + bo;
+            }
+            if constexpr (kNext) {
+              if (p.next_relu) y = fmaxf(y, 0.0f);
+            }
+            const uint32_t h = __half_as_ushort(__float2half_rn(y));
+            if constexpr (kNext) {
+              if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
+            }
+            yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
+          }
+          box_reuse_wait(lane);
+          box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
+                        n0 + j0, lane);
+          slot ^= 1u;
+          if constexpr (kDebug) {
+  #pragma unroll 1
+            for (int j = 0; j < kW; ++j) {
+              const int tok = n0 + j0 + j;
+              if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = accv[j];
+            }
+          }
+          if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales
+  #pragma unroll
+            for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
+            if constexpr (kZp) {
+  #pragma unroll
+              for (int i = 0; i + 1 < kNR; ++i) za[i] = za[i + 1];
+            }
+          }
+        };
+
+        for (int si = 0; si < nseg_tile && ok; ++si, ++nseg) {
+          const bool is_out = si >= nseg_int;
+          const bool first = si == 0;
+          const bool last = si == nseg_tile - 1;
+          const uint32_t b = nseg & 1u;
+          if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
+          tc_fence_after();
+          const uint32_t tF = tq + b * BN;
+          // Running sums of the piece (not for its first segment): slice j0's are in pc
+          // while the next slice's load into pn, so the L2 latency is paid once per segment.
+          int pn[kW];
+  #pragma unroll
+          for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
+  #pragma unroll 1
           for (int j0 = 0; j0 < BN; j0 += kW) {
             int pc[kW];
-#pragma unroll
+  #pragma unroll
             for (int j = 0; j < kW; ++j) pc[j] = pn[j];
             if (!first && j0 + kW < BN) {
-#pragma unroll
+  #pragma unroll
               for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
             }
             uint32_t f[kW];
@@ -470,73 +742,77 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&tmem_empty[b]);
             }
-            const float ra_s = ra[0];  // this slice's tokens, one per lane
-            [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
-            uint32_t yh[kW / 2];
-#pragma unroll
+            if (!last) {
+              // an int segment that is not the last one of the piece: fold it into the
+              // running sum (first segment: store it)
+  #pragma unroll
+              for (int j = 0; j < kW; ++j)
+                accs[(size_t)(j0 + j) * 128] = pc[j] + __float2int_rn(__uint_as_float(f[j]));
+              continue;
+            }
+            int accv[kW];
+            float fov[kW];
+  #pragma unroll
             for (int j = 0; j < kW; ++j) {
-              int acc;
-              float fo = 0.0f;
-              if (is_out) {
-                acc = pc[j];
-                fo = __uint_as_float(f[j]);
-              } else {
-                acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
-              }
-              const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
-              float y;
-              if constexpr (kZp) {
-                // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
-                // when |Z| <= z_safe bounds it below 2^31 (token j is the same for the
-                // whole warp, so the branch is uniform), in 64 bits otherwise
-                const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
-                if (abs(zj) <= p.z_safe) {
-                  y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
-                } else {
-                  const long long az = (long long)acc + (long long)zj * (long long)cbin;
-                  y = __ll2float_rn(az) * (rj * so) + fo + bo;
-                }
-              } else {
-                y = (float)acc * (rj * so) + fo + bo;
-              }
-              if constexpr (kNext) {
-                if (p.next_relu) y = fmaxf(y, 0.0f);
-              }
-              const uint32_t h = __half_as_ushort(__float2half_rn(y));
-              if constexpr (kNext) {
-                if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
-              }
-              yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
-              if constexpr (kDebug) pc[j] = acc;
+              accv[j] = is_out ? pc[j] : pc[j] + __float2int_rn(__uint_as_float(f[j]));
+              fov[j] = is_out ? __uint_as_float(f[j]) : 0.0f;
             }
-            box_reuse_wait(lane);
-            box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
-                          n0 + j0, lane);
-            slot ^= 1u;
-            if constexpr (kDebug) {
-#pragma unroll 1
+            if (whole) {
+              emit(j0, accv, fov);
+            } else {
+  #pragma unroll
               for (int j = 0; j < kW; ++j) {
-                const int tok = n0 + j0 + j;
-                if (o_ok && tok < p.T) p.acc_debug[(size_t)tok * p.out + o] = pc[j];
+                my_part[(size_t)(j0 + j) * 128] = accv[j];
+                if (has_out) my_part_f[(size_t)(j0 + j) * 128] = fov[j];
               }
             }
-            if ((j0 + kW) % 32 == 0) {  // next 32 tokens: rotate the prefetched row scales
-#pragma unroll
-              for (int i = 0; i + 1 < kNR; ++i) ra[i] = ra[i + 1];
-              if constexpr (kZp) {
-#pragma unroll
-                for (int i = 0; i + 1 < kNR; ++i) za[i] = za[i + 1];
-              }
-            }
-          }
-          if constexpr (kNext) {  // the tile's flags of columns m0 + 32q .. + 31
-            const uint32_t word = __ballot_sync(0xffffffffu, o_ok && ymax >= p.next_thr);
-            if (lane == 0 && word != 0u) atomicOr(&p.next_mask[(m0 + 32 * q) >> 5], word);
           }
         }
+        if (!ok) break;
+        if (!whole) {
+          // arrive on the tile; the last of its pieces (b_first .. b_last) finishes it
+          const long long ut0 = (long long)t * p.nchunks;
+          const int b_first = unit_owner(p, ut0);
+          const int b_last = unit_owner(p, ut0 + p.nchunks - 1);
+          __threadfence();  // this thread's part stores before the arrival (all four warps)
+          if (!(ok = epi_sync())) break;
+          if (q == 0 && lane == 0) {
+            __threadfence();
+            *s_fin = atomicAdd(&p.tile_cnt[t], 1) == b_last - b_first ? 1 : 0;
+          }
+          if (!(ok = epi_sync())) break;
+          if (*s_fin) {
+            __threadfence();
+            const bool t_out = nkb_out > 0;
+            const float* pf = p.part_f + (size_t)b_last * BN * 128 + 32 * q + lane;
+  #pragma unroll 1
+            for (int j0 = 0; j0 < BN; j0 += kW) {
+              int accv[kW];
+              float fov[kW];
+  #pragma unroll
+              for (int j = 0; j < kW; ++j) {
+                accv[j] = 0;
+                fov[j] = t_out ? __ldcg(pf + (size_t)(j0 + j) * 128) : 0.0f;
+              }
+  #pragma unroll 1
+              for (int bb = b_first; bb <= b_last; ++bb) {
+                const int ps = unit_start(p, bb) >= ut0 ? 0 : 1;
+                const int32_t* src =
+                    p.part + ((size_t)bb * 2 + ps) * BN * 128 + 32 * q + lane + (size_t)j0 * 128;
+  #pragma unroll
+                for (int j = 0; j < kW; ++j) accv[j] += __ldcg(src + (size_t)j * 128);
+              }
+              emit(j0, accv, fov);
+            }
+          }
+        }
+        if constexpr (kNext) {  // the tile's flags of columns m0 + 32q .. + 31
+          const uint32_t word = __ballot_sync(0xffffffffu, o_ok && ymax >= p.next_thr);
+          if (lane == 0 && word != 0u) atomicOr(&p.next_mask[(m0 + 32 * q) >> 5], word);
+        }
       }
+      if (lane == 0) bulk_wait_group0();  // output stores complete before the CTA exits
     }
-    if (lane == 0) bulk_wait_group0();  // output stores complete before the CTA exits
   }
 
   // -------------------------------------------------------- teardown
@@ -546,16 +822,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
+template <int BN, int kMode, bool kSplit>
+cudaError_t launch_split(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
+                         const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
+                         const Params& p, int grid) {
+  using C = Cfg<BN>;
+  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kMode, kSplit>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
+  if (e != cudaSuccess) return e;
+  i8_gemm_kernel<BN, kMode, kSplit><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
+  return cudaGetLastError();
+}
+
 template <int BN, int kMode>
 cudaError_t launch_kernel(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
                           const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
                           const Params& p, int grid) {
-  using C = Cfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kMode>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
-  if (e != cudaSuccess) return e;
-  i8_gemm_kernel<BN, kMode><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
-  return cudaGetLastError();
+  if (p.split) return launch_split<BN, kMode, true>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  return launch_split<BN, kMode, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
 }
 
 template <int BN>
@@ -609,7 +893,17 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.timeout_ns = a.timeout_ns;
   p.debug_skip_loads = a.debug_skip_loads;
   const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < kSmCount ? tiles : kSmCount;
+  int grid = tiles < kSmCount ? tiles : kSmCount;
+  p.split = 0;
+  if (a.split) {  // cut tiles between CTAs by 1024-K chunks (see i8_split_ctas)
+    if (!a.part || !a.part_f || !a.tile_cnt) return cudaErrorInvalidValue;
+    p.split = 1;
+    p.units = (long long)tiles * p.nchunks;
+    p.part = a.part;
+    p.part_f = a.part_f;
+    p.tile_cnt = a.tile_cnt;
+    grid = a.split;
+  }
   // ReLU comes only with the statistics epilogue (an FFN's up projection)
   if ((a.next.relu && !a.next.mask) || (a.next.mask && (a.acc_debug || a.zi)))
     return cudaErrorInvalidValue;

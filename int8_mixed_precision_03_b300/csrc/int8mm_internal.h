@@ -21,6 +21,29 @@ inline int i8_bn(int T) {
 }
 inline int num_chunks(int in) { return (in + kChunkK - 1) / kChunkK; }
 
+// Work split of the tensor-core matmul. Unsplit, CTA b of G = min(tiles, 148) takes the
+// whole tiles b, b + G, ...; the slowest CTA does ceil(tiles / G) tiles of `chunks`
+// 1024-K chunks each. Split, the (tile, chunk) units are cut into G = min(units, 148)
+// contiguous ranges (ceil(units / G) units at most). A tile cut into pieces costs its
+// epilogue warps a second pass (the pieces' sums are published and the last piece to
+// arrive adds them up), which the epilogue of a 128- or 256-token tile cannot hide:
+// measured on B300, splitting the 13B up and down projections (critical path -3% and
+// -13%) made them 20% and 15% slower, while the 64-token decode tile gained 11%. Returns
+// the split's CTA count when it shortens the slowest CTA's work by more than 3% (token
+// tiles up to 64) or 25% (larger tiles), else 0 (unsplit).
+inline int i8_split_ctas(int T, int in, int out) {
+  const int bn = i8_bn(T);
+  const long long tiles = (long long)((out + 127) / 128) * ((T + bn - 1) / bn);
+  const long long chunks = num_chunks(in);
+  if (tiles <= 0 || chunks <= 1) return 0;
+  const long long g0 = tiles < kSmCount ? tiles : kSmCount;
+  const long long whole = (tiles + g0 - 1) / g0 * chunks;
+  const long long units = tiles * chunks;
+  const long long g1 = units < kSmCount ? units : kSmCount;
+  const long long cut = (units + g1 - 1) / g1;
+  return cut * 100 < whole * (bn <= 64 ? 97 : 75) ? (int)g1 : 0;
+}
+
 // Device status header at the start of every int8_matmul workspace (zeroed per call).
 struct WsHeader {
   int32_t status;         // first device-side error (i8_status), 0 if none
@@ -38,6 +61,10 @@ struct WsLayout {
   size_t zi = 0;          // zeropoint variant: int32 per-row zero points [T]
   size_t cbout = 0;       // zeropoint variant: int32 sums of the outlier columns' codes [out]
   size_t acc = 0;         // int32 running sums of the matmul's epilogue, one tile per SM
+  // split work (i8_split_ctas > 0): per-tile arrival counters (zeroed with the header),
+  // the pieces' int32 sums [G][2][BN][128] and outlier sums [G][BN][128]
+  size_t tile_cnt = 0, part = 0, part_f = 0;
+  int split = 0;          // the split's CTA count, 0 if unsplit
   size_t total = 0;
   size_t zero_bytes = 0;  // header + mask + l1: memset at the start of every call
   int words = 0;          // 32-column words of the outlier mask
@@ -46,7 +73,8 @@ struct WsLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int T, int in, int out, int ncap) {
+// split_ok = false: the layout of the unsplit schedule (no split sections).
+inline WsLayout ws_layout(int T, int in, int out, int ncap, bool split_ok = true) {
   WsLayout L;
   size_t off = 0;
   L.words = (in + 31) / 32;
@@ -57,6 +85,11 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.l1 = off;
   off = align_up(off + sizeof(int32_t) * (size_t)((T + i8_bn(T) - 1) / i8_bn(T)) *
                            num_chunks(in), 256);
+  L.split = split_ok ? i8_split_ctas(T, in, out) : 0;
+  L.tile_cnt = off;
+  if (L.split)
+    off = align_up(off + sizeof(int32_t) * (size_t)((out + 127) / 128) *
+                             ((T + i8_bn(T) - 1) / i8_bn(T)), 256);
   L.zero_bytes = off;
   L.idx = off; off = align_up(off + sizeof(int32_t) * (size_t)in, 256);
   L.xq = off; off = align_up(off + 2 * (size_t)T * in, 256);
@@ -66,6 +99,10 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap) {
   L.zi = off; off = align_up(off + 4 * (size_t)T, 256);
   L.cbout = off; off = align_up(off + 4 * (size_t)out, 256);
   L.acc = off; off = align_up(off + 4 * (size_t)kSmCount * 128 * i8_bn(T), 256);
+  L.part = off;
+  if (L.split) off = align_up(off + 4 * (size_t)L.split * 2 * 128 * i8_bn(T), 256);
+  L.part_f = off;
+  if (L.split) off = align_up(off + 4 * (size_t)L.split * 128 * i8_bn(T), 256);
   L.total = off;
   return L;
 }
@@ -140,6 +177,11 @@ struct GemmArgs {
   const int32_t* zi = nullptr;
   const int32_t* cbsum = nullptr;
   const int32_t* cbout = nullptr;
+  // split work (split = CTA count, 0: whole tiles per CTA); see WsLayout
+  int split = 0;
+  int32_t* part = nullptr;
+  float* part_f = nullptr;
+  int32_t* tile_cnt = nullptr;
   int relu = 0;                 // fp16 comparator: ReLU on Y
   uint64_t timeout_ns = 2000000000ull;
   int debug_skip_loads = 0;     // test hook: the producer issues nothing (waits time out)

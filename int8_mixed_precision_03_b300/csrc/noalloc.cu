@@ -46,10 +46,12 @@ i8_status scratch_for_current_device(void** addr) {
 I8_API i8_status int8_matmul_noalloc(const void* X, int T, int in, const int8_t* CB,
                                      const float* SCB, int out, float threshold,
                                      const void* bias, void* Y, void* stream) {
-  // the smallest workspace int8_matmul accepts: a 64-column outlier capacity
-  const size_t need = int8_matmul_workspace_size(T, in, out, 64);
-  if (need == 0)  // invalid sizes: the regular entry point reports them, launching nothing
+  // the smallest workspace int8_matmul accepts: a 64-column outlier capacity, unsplit
+  // schedule (int8_matmul takes the split one when the scratch also holds its slots)
+  if (int8_matmul_workspace_size(T, in, out, 64) == 0)
+    // invalid sizes: the regular entry point reports them, launching nothing
     return int8_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, nullptr, 0, stream);
+  const size_t need = i8mm::ws_layout(T, in, out, 64, false).total;
   if (need > I8_NOALLOC_SCRATCH_BYTES) return I8_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const i8_status st = scratch_for_current_device(&ws);

@@ -278,3 +278,31 @@ def test_stalled_matmul_times_out_and_the_context_stays_usable(i8):
     assert rc == 0
     assert i8.i8_get_status(ws) == 7  # I8_ERR_TIMEOUT
     run_and_compare(i8, X, W, bias, 6.0)
+
+
+# ----------------------------------------------------------------- split schedule
+@pytest.mark.parametrize("T,d,out,k", [
+    (64, 2064, 128, 17),      # one tile cut into three single-chunk pieces
+    (300, 3072, 640, 40),     # ten tiles over 30 CTAs
+    (64, 14336, 8192, 14),    # decode-like tile of 64 tokens, 14 chunks per tile
+    (200, 5120, 2560, 10),    # pieces of several chunks
+])
+def test_split_and_unsplit_schedules_agree_bit_for_bit(i8, T, d, out, k):
+    """Tiles cut between CTAs (the split schedule, used with a full-size workspace) give the
+    same Y, bit for bit, as whole tiles per CTA (the schedule a workspace without the split
+    slots falls back to): the int32 sums are exact and each piece's outlier sums come
+    from one CTA."""
+    w = synth.Workload("split", T, d, out, n_outlier_cols=k, row_frac=0.8, seed=T + d + out)
+    X, W, bias = dev(synth.make_x(w)), dev(synth.make_w(w)), dev(synth.make_bias(w))
+    CB, SCB = i8.int8_quantize_weight(W)
+    full = i8.int8_matmul_workspace_size(T, d, out, 64)
+    ws_split = torch.empty(full, dtype=torch.uint8, device="cuda")
+    ws_whole = torch.empty(full - 1, dtype=torch.uint8, device="cuda")
+    Y1 = i8.int8_matmul(X, CB, SCB, 6.0, bias, workspace=ws_split)
+    Y2 = i8.int8_matmul(X, CB, SCB, 6.0, bias, workspace=ws_whole)
+    assert i8.i8_get_status(ws_split) == 0 and i8.i8_get_status(ws_whole) == 0
+    assert torch.equal(Y1, Y2)
+    sums = i8.int8_weight_code_sums(CB)
+    Z1 = i8.int8_matmul_zeropoint(X, CB, SCB, sums, 6.0, bias, workspace=ws_split)
+    Z2 = i8.int8_matmul_zeropoint(X, CB, SCB, sums, 6.0, bias, workspace=ws_whole)
+    assert torch.equal(Z1, Z2)

@@ -109,8 +109,9 @@ def test_full_size_6p7b_sampled_rows(i8):
 
 
 def test_rows_far_from_zero_take_the_64_bit_correction(i8):
-    """Inlier rows in [5, 5.016): S = 32512, Z = 162687, beyond the bound up to which the
-    epilogue adds Z * (code sum) in 32-bit integers; those tokens take the 64-bit path."""
+    """Inlier rows in [5, 5.015625]: S = 16256, Z = 81407, beyond the bound (16386 for
+    in = 1024) up to which the epilogue adds Z * (code sum) in 32-bit integers; those tokens
+    take the 64-bit path."""
     w = synth.Workload("far", 40, 1024, 384, n_outlier_cols=2, seed=12)
     X = synth.make_x(w)
     g = np.random.default_rng(5)
@@ -119,5 +120,5 @@ def test_rows_far_from_zero_take_the_64_bit_correction(i8):
         X[r, inl] = (5.0 + g.integers(0, 3, inl.size) / 128.0).astype(np.float16)
         X[r, inl[:2]] = [5.0, 5.015625]
     r, ref = run_and_compare(i8, X, synth.make_w(w), synth.make_bias(w), 6.0)
-    assert (ref["Z"][[0, 7, 39]] == 162687).all()
+    assert (ref["Z"][[0, 7, 39]] == 81407).all()
     assert np.abs(ref["Z"]).max() > (2**31 - 1 - 16129 * 1024) // (127 * 1024)
