@@ -234,17 +234,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
-def calibrated_rows(w, X, CBo, SCBo, bias, nthreads: int, seconds: float) -> int:
+def oracle_matmul(zeropoint: bool):
+    """The oracle's matmul: absmax codes, or the zeropoint variant."""
+    import oracle
+    return oracle.int8_matmul_zeropoint if zeropoint else oracle.int8_matmul
+
+
+def calibrated_rows(w, X, CBo, SCBo, bias, nthreads: int, seconds: float,
+                    zeropoint: bool = False) -> int:
     """Rows of X whose oracle evaluation takes about `seconds` on these host cores: the
     per-row cost is the slope between two timed samples (the fixed cost of a call, the
     outlier scan over all of X, cancels)."""
-    import oracle
+    fn = oracle_matmul(zeropoint)
 
     def timed(n):
         rows = np.linspace(0, w.T - 1, n).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.int8_matmul(X, CBo, SCBo, w.threshold, bias, rows=rows, nthreads=nthreads,
-                           want_acc=False)
+        fn(X, CBo, SCBo, w.threshold, bias, rows=rows, nthreads=nthreads, want_acc=False)
         return time.perf_counter() - t0
 
     n1, n2 = min(w.T, 4 * nthreads), min(w.T, 16 * nthreads)
@@ -254,24 +260,49 @@ def calibrated_rows(w, X, CBo, SCBo, bias, nthreads: int, seconds: float) -> int
     return int(min(w.T, max(1, round((seconds - fixed) / per_row))))
 
 
-def cpu_baseline_sample(w, X, CBo, SCBo, bias, nthreads: int, seconds: float = 15.0) -> dict:
+def cpu_baseline_sample(w, X, CBo, SCBo, bias, nthreads: int, seconds: float = 15.0,
+                        zeropoint: bool = False) -> dict:
     """The oracle as it stands, timed on a bounded sample of rows of the workload."""
-    import oracle
-    rows_n = calibrated_rows(w, X, CBo, SCBo, bias, nthreads, seconds)
+    fn = oracle_matmul(zeropoint)
+    rows_n = calibrated_rows(w, X, CBo, SCBo, bias, nthreads, seconds, zeropoint)
     rows = np.linspace(0, w.T - 1, rows_n).astype(np.int64)
     reps, t0 = 0, time.perf_counter()
     while True:   # the whole workload may take less than `seconds`: repeat it
-        oracle.int8_matmul(X, CBo, SCBo, threshold=w.threshold, bias=bias, rows=rows,
-                           nthreads=nthreads, want_acc=False)
+        fn(X, CBo, SCBo, w.threshold, bias, rows=rows, nthreads=nthreads, want_acc=False)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= 0.6 * seconds:
             break
     ops = 2.0 * rows_n * w.d_in * w.d_out * reps
+    codes = "zeropoint" if zeropoint else "absmax"
     return {"value": ops / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{reps} x {rows_n} of {w.T} rows of {w.name} (each pass: outlier scan "
-                      f"of all of X, then quantize, int8 product, fp16 outlier product and "
-                      f"bias for those rows), {dt:.1f} s wall"}
+                      f"of all of X, then {codes} quantize, int8 product, fp16 outlier product "
+                      f"and bias for those rows), {dt:.1f} s wall"}
+
+
+def ffn_cpu_baseline(f, blk, nthreads: int, seconds: float = 15.0) -> dict:
+    """The oracle's FFN block as it stands on the first rows of X (a smaller batch of the
+    same block: the down projection's outlier columns need every row of its input, so the
+    sample is a batch, not a row subset), sized to about `seconds`, scaled to TOPS."""
+    import oracle
+    CBu, SCBu = oracle.quantize_weight(blk["W_up"])
+    CBd, SCBd = oracle.quantize_weight(blk["W_down"])
+
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.ffn(blk["X"][:n], CBu, SCBu, CBd, SCBd, f.threshold, blk["b_up"], blk["b_down"],
+                   "relu", nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    n1 = min(f.T, 2 * nthreads)
+    t1 = run(n1)
+    n = int(min(f.T, max(n1, round(n1 * seconds / max(t1, 1e-3)))))
+    dt = run(n) if n != n1 else t1
+    return {"value": 4.0 * n * f.d_model * f.d_ff / dt / 1e12, "unit": UNIT,
+            "cores": nthreads, "kind": "oracle",
+            "sample": f"the first {n} of {f.T} tokens of {f.name} through the whole block "
+                      f"(both outlier scans, quantize, int8 products, ReLU), {dt:.1f} s wall"}
 
 
 def run_reference(args) -> None:
@@ -475,10 +506,11 @@ def run_ours(args) -> None:
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline and not zp:
+    if world == 1 and not args.no_cpu_baseline:
         import oracle
         CBo, SCBo = oracle.quantize_weight(Wh)
-        line["cpu_baseline"] = cpu_baseline_sample(w, Xh, CBo, SCBo, bh, os.cpu_count() or 1)
+        line["cpu_baseline"] = cpu_baseline_sample(w, Xh, CBo, SCBo, bh, os.cpu_count() or 1,
+                                                   zeropoint=zp)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -640,6 +672,8 @@ def run_ffn(args) -> None:
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = ffn_cpu_baseline(f, blk, os.cpu_count() or 1)
     print(json.dumps(line), flush=True)
 
 
