@@ -46,6 +46,12 @@
 // for the weight stream, warps 4-7 and 12-15 converters, warps 8-11 epilogue (warp w
 // reaches TMEM lanes 32*(w%4) .. +31). Persistent CTAs, one per SM, walk tiles
 // token-block fastest so that concurrently running CTAs share the same weight strip in L2.
+//
+// Schedules: whole tiles per CTA (t = b, b + G, ...), or, where that leaves the last wave
+// unbalanced (i8_split_ctas), the split schedule (kSplit): the (tile, 1024-K chunk) units
+// are cut into one contiguous range per CTA, and a tile cut into pieces is finished by the
+// last of its pieces to arrive, from the exact int32 sums (and the tile-ending piece's fp32
+// outlier sums) the pieces leave in their CTAs' slots. No CTA ever waits for another.
 #include "gemm_common.cuh"
 
 namespace i8mm {
