@@ -97,3 +97,19 @@ def test_rewritten_model_keeps_the_head_in_fp16(i8):
     h = i8.int8_matmul(h, CB2, S2, 6.0, ref["fc2.bias"].cuda())
     y2 = torch.nn.functional.linear(h, ref["lm_head.weight"].cuda(), ref["lm_head.bias"].cuda())
     assert torch.equal(y, y2)
+
+
+def test_pages_example_two_64_by_64_layers(i8):
+    """The two 64 x 64 layers of the transformers-integration example, moved to the GPU:
+    each layer is quantized there and the model's output is the chain of the two calls."""
+    torch.manual_seed(3)
+    fp16_model = torch.nn.Sequential(torch.nn.Linear(64, 64), torch.nn.Linear(64, 64)).half()
+    ref = {k: v.clone() for k, v in fp16_model.state_dict().items()}
+    int8_model = replace_8bit_linear(fp16_model).to("cuda")
+    assert all(m.quantized for m in int8_model)
+    x = torch.from_numpy(synth.make_random_f16(4, (8, 64))).cuda()
+    y = int8_model(x)
+    CB0, S0 = i8.int8_quantize_weight(ref["0.weight"].cuda())
+    CB1, S1 = i8.int8_quantize_weight(ref["1.weight"].cuda())
+    h = i8.int8_matmul(x, CB0, S0, 6.0, ref["0.bias"].cuda())
+    assert torch.equal(y, i8.int8_matmul(h, CB1, S1, 6.0, ref["1.bias"].cuda()))

@@ -75,3 +75,16 @@ def test_meta_construction_and_no_cpu_path():
     c = Linear8bitLt(64, 128)
     with pytest.raises(RuntimeError):
         c(torch.zeros(2, 64, dtype=torch.float16))
+
+
+def test_pages_example_two_64_by_64_layers_are_replaced():
+    """The transformers-integration example: a model of two 64 x 64 linear layers, both
+    replaced (neither is named lm_head), fp16 weights kept until the model moves to a GPU."""
+    torch.manual_seed(3)
+    fp16_model = torch.nn.Sequential(torch.nn.Linear(64, 64), torch.nn.Linear(64, 64)).half()
+    ref = [m.weight.detach().clone() for m in fp16_model]
+    int8_model = replace_8bit_linear(fp16_model, threshold=6.0)
+    assert all(isinstance(m, Linear8bitLt) for m in int8_model)
+    assert all(not m.quantized and m.weight.dtype == torch.float16 for m in int8_model)
+    for m, w in zip(int8_model, ref):
+        assert torch.equal(m.weight, w)
