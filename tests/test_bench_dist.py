@@ -73,3 +73,51 @@ def test_matmul_path_selection_follows_the_library_rule():
     assert bench.matmul_kernel(synth.WORKLOADS["tiny"]) == "gemv_mma_kernel"
     assert bench.matmul_kernel(synth.WORKLOADS["decode_176b_t64"]) == "i8_gemm_kernel"
     assert bench.matmul_kernel(synth.WORKLOADS["ffn_6.7b_up"]) == "i8_gemm_kernel"
+
+
+def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    import bench
+    src = "// header\nint f(int a) {  /* inline */ return a + 1; }\n\n// tail\n"
+    for name in ("a.cu", "b.h"):
+        (tmp_path / name).write_text(src)
+    monkeypatch.setattr(bench, "CSRC", str(tmp_path))
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "k", ("a.cu", "b.h"))
+    h0 = bench.kernel_source_hash("k")
+    (tmp_path / "a.cu").write_text("// other words\n" + src + "\n// more\n")
+    assert bench.kernel_source_hash("k") == h0
+    (tmp_path / "a.cu").write_text(src.replace("a + 1", "a + 2"))
+    assert bench.kernel_source_hash("k") != h0
+
+
+def test_roofline_bound_and_fraction_follow_the_workload():
+    import bench
+    import synth
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1500.0}
+    w = synth.WORKLOADS["decode_176b_t8"]
+    r = bench.roofline(w, 0.2, peaks, "test")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - bench.matmul_bytes(w) / 0.2e-3 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 6000.0) < 1e-12
+    w = synth.WORKLOADS["ffn_6.7b_up"]
+    r = bench.roofline(w, 0.25, peaks, "test")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - bench.workload_ops(w) / 0.25e-3 / 1e12) < 1e-9
+    # the zeropoint variant runs on the tensor-core kernel at every size; no traffic record
+    r = bench.roofline(synth.WORKLOADS["decode_176b_t8"], 0.2, peaks, "test", zeropoint=True)
+    assert r["kernel"].startswith("i8_gemm_kernel") and r["traffic"] is None
+
+
+def test_cpu_baselines_run_the_oracle_on_bounded_samples():
+    import bench
+    import oracle
+    import synth
+    w = synth.WORKLOADS["tiny"]
+    X, W, b = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    CB, SCB = oracle.quantize_weight(W)
+    for zp in (False, True):
+        r = bench.cpu_baseline_sample(w, X, CB, SCB, b, 2, seconds=0.2, zeropoint=zp)
+        assert r["kind"] == "oracle" and r["cores"] == 2 and r["value"] > 0
+        assert ("zeropoint" in r["sample"]) == zp
+    f = synth.FFN_WORKLOADS["ffn_small"].with_(T=24)
+    r = bench.ffn_cpu_baseline(f, synth.make_ffn(f), 2, seconds=0.2)
+    assert r["kind"] == "oracle" and r["value"] > 0 and "of 24 tokens" in r["sample"]
