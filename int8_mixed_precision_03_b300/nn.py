@@ -43,7 +43,8 @@ class Linear8bitLt(torch.nn.Module):
     quantized) and `bias`; an int8 state dict loads as it is, an fp16 one is quantized on
     load when the layer is on the GPU. `max_outlier_cols` bounds the outlier columns the
     workspace holds (0: all of `in_features`); more than that is reported in the workspace
-    status word, not raised."""
+    status word, not raised. A threshold <= 0 turns the decomposition off (stored as +inf,
+    plain vector-wise int8), since the library takes only positive thresholds."""
 
     def __init__(self, in_features: int, out_features: int, bias: bool = True,
                  has_fp16_weights: bool = False, threshold: float = 6.0, device=None,
@@ -53,7 +54,7 @@ class Linear8bitLt(torch.nn.Module):
             raise ValueError("in_features must be a multiple of 16")
         self.in_features, self.out_features = in_features, out_features
         self.has_fp16_weights = has_fp16_weights
-        self.threshold = float(threshold)
+        self.threshold = float(threshold) if threshold > 0 else math.inf
         self.max_outlier_cols = max_outlier_cols
         w = torch.empty(out_features, in_features, dtype=torch.float16, device=device)
         if w.device.type != "meta":  # the initialisation of nn.Linear

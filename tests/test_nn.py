@@ -88,3 +88,9 @@ def test_pages_example_two_64_by_64_layers_are_replaced():
     assert all(not m.quantized and m.weight.dtype == torch.float16 for m in int8_model)
     for m, w in zip(int8_model, ref):
         assert torch.equal(m.weight, w)
+
+
+def test_threshold_zero_turns_the_decomposition_off():
+    assert Linear8bitLt(32, 16, threshold=0.0).threshold == float("inf")
+    assert Linear8bitLt(32, 16, threshold=-1.0).threshold == float("inf")
+    assert Linear8bitLt(32, 16).threshold == 6.0
