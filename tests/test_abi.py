@@ -186,3 +186,15 @@ def test_zeropoint_entry_points_validate(L):
     assert L.int8_weight_code_sums(p, 4, 16, fake(A + 2), None) == 2
     assert L.int8_weight_code_sums(p, 0, 16, p, None) == 0
     assert L.i8_last_launch_count() == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    """No CPU fallback: with the shared library missing, the binding raises."""
+    monkeypatch.setattr(i8, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(i8, "_lib", None)
+    with pytest.raises(ImportError):
+        i8.lib()
+    import torch
+    with pytest.raises((ImportError, ValueError)):
+        i8.int8_matmul(torch.zeros(2, 16, dtype=torch.float16),
+                       torch.zeros(4, 16, dtype=torch.int8), torch.ones(4))
