@@ -170,7 +170,7 @@ cudaError_t launch_colstats(const void* X, int T, int in, uint16_t thr_bits, WsH
                             uint32_t* mask, int32_t* idx, int ncap, cudaStream_t s) {
   const int colblocks = (in + kColsPerCta - 1) / kColsPerCta;
   // about four CTAs per SM in total, at least 8 rows per split
-  int splits = (4 * kSmCount + colblocks - 1) / colblocks;
+  int splits = (4 * sm_count() + colblocks - 1) / colblocks;
   splits = max(1, min(splits, (T + 7) / 8));
   const int rows_per_split = (T + splits - 1) / splits;
   splits = (T + rows_per_split - 1) / rows_per_split;

@@ -215,7 +215,8 @@ cudaError_t launch_f16_bn(const GemmArgs& a, cudaStream_t s) {
   p.relu = a.relu;
   p.timeout_ns = a.timeout_ns;
   const int tiles = p.m_tiles * p.n_tiles;
-  const int grid = tiles < kSmCount ? tiles : kSmCount;
+  const int sms = sm_count();
+  const int grid = tiles < sms ? tiles : sms;
   cudaError_t e = cudaFuncSetAttribute(f16_gemm_kernel<BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
   if (e != cudaSuccess) return e;

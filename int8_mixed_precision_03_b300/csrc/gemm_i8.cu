@@ -899,7 +899,8 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.timeout_ns = a.timeout_ns;
   p.debug_skip_loads = a.debug_skip_loads;
   const int tiles = p.m_tiles * p.n_tiles;
-  int grid = tiles < kSmCount ? tiles : kSmCount;
+  const int sms = sm_count();
+  int grid = tiles < sms ? tiles : sms;
   p.split = 0;
   if (a.split) {  // cut tiles between CTAs by 1024-K chunks (see i8_split_ctas)
     if (!a.part || !a.part_f || !a.tile_cnt) return cudaErrorInvalidValue;

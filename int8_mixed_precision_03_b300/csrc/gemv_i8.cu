@@ -223,8 +223,10 @@ __global__ void __launch_bounds__(GvShape<T>::kThreads, 1) gemv_i8_kernel(
 
 // Shared memory of the kernel: x codes, the outlier-byte table (if use_tab) and X_out.
 size_t gemv_smem(int T, int in, int out, bool use_tab) {
-  // a CTA owns floor((b+1)*out/kSmCount) - floor(b*out/kSmCount) <= ceil(out/kSmCount) rows
-  const int rows_cta = (out + kSmCount - 1) / kSmCount;
+  // with G = sm_count() CTAs, a CTA owns floor((b+1)*out/G) - floor(b*out/G) <= ceil(out/G)
+  // rows
+  const int G = sm_count();
+  const int rows_cta = (out + G - 1) / G;
   size_t b = (size_t)T * in;
   if (use_tab) b += align16((size_t)rows_cta * kOutTab) + (size_t)T * kOutTab * 4;
   return b;
@@ -237,7 +239,7 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gemv_i8_kernel<T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  gemv_i8_kernel<T><<<kSmCount, GvShape<T>::kThreads, smem, s>>>(
+  gemv_i8_kernel<T><<<sm_count(), GvShape<T>::kThreads, smem, s>>>(
       a.CB, a.SCB, a.in, a.out, a.xq8, a.rowabs, a.hdr, a.idx,
       static_cast<const uint16_t*>(a.xout), a.ncap, static_cast<const uint16_t*>(a.bias),
       static_cast<uint16_t*>(a.Y), a.acc_debug, use_tab ? 1 : 0, a.next);

@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(kMvThreads, 1) gemv_mma_kernel(
 }
 
 size_t mv_smem(int T, int in, int out, bool use_tab) {
-  const int rows_cta = (out + kSmCount - 1) / kSmCount;
+  const int G = sm_count();  // the grid of launch_nt
+  const int rows_cta = (out + G - 1) / G;
   size_t b = mv_align16((size_t)T * mv_xstride(in));
   if (use_tab) b += mv_align16((size_t)rows_cta * kMvTab) + (size_t)T * kMvTab * 4;
   return b;
@@ -228,7 +229,7 @@ cudaError_t launch_nt(const GemvArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  gemv_mma_kernel<NT><<<kSmCount, kMvThreads, smem, s>>>(
+  gemv_mma_kernel<NT><<<sm_count(), kMvThreads, smem, s>>>(
       a.CB, a.SCB, a.T, a.in, a.out, a.xq8, a.rowabs, a.hdr, a.idx,
       static_cast<const uint16_t*>(a.xout), a.ncap, static_cast<const uint16_t*>(a.bias),
       static_cast<uint16_t*>(a.Y), a.acc_debug, use_tab ? 1 : 0, a.next);

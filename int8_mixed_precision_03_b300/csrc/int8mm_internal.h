@@ -8,7 +8,12 @@
 
 namespace i8mm {
 
-constexpr int kSmCount = 148;       // B300: 2 dies x 74 SMs
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount, looked
+// up once per device). The persistent grids, the split plan and the per-SM workspace slots
+// are sized from it. Without a usable device (workspace sizing on a host with no GPU) it
+// returns kSmFallback, B300's count (2 dies x 74 SMs).
+constexpr int kSmFallback = 148;
+int sm_count();
 constexpr int kKBlock = 64;         // K elements per pipeline stage (128 bytes of fp16)
 constexpr int kChunkKBlocks = 16;   // K blocks per exact fp32 accumulation chunk (1024 K)
 constexpr int kChunkK = kKBlock * kChunkKBlocks;
@@ -36,10 +41,11 @@ inline int i8_split_ctas(int T, int in, int out) {
   const long long tiles = (long long)((out + 127) / 128) * ((T + bn - 1) / bn);
   const long long chunks = num_chunks(in);
   if (tiles <= 0 || chunks <= 1) return 0;
-  const long long g0 = tiles < kSmCount ? tiles : kSmCount;
+  const long long sms = sm_count();
+  const long long g0 = tiles < sms ? tiles : sms;
   const long long whole = (tiles + g0 - 1) / g0 * chunks;
   const long long units = tiles * chunks;
-  const long long g1 = units < kSmCount ? units : kSmCount;
+  const long long g1 = units < sms ? units : sms;
   const long long cut = (units + g1 - 1) / g1;
   return cut * 100 < whole * (bn <= 64 ? 97 : 75) ? (int)g1 : 0;
 }
@@ -98,7 +104,7 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap, bool split_ok = true
   L.wout = off; off = align_up(off + 2 * (size_t)out * ncap, 256);
   L.zi = off; off = align_up(off + 4 * (size_t)T, 256);
   L.cbout = off; off = align_up(off + 4 * (size_t)out, 256);
-  L.acc = off; off = align_up(off + 4 * (size_t)kSmCount * 128 * i8_bn(T), 256);
+  L.acc = off; off = align_up(off + 4 * (size_t)sm_count() * 128 * i8_bn(T), 256);
   L.part = off;
   if (L.split) off = align_up(off + 4 * (size_t)L.split * 2 * 128 * i8_bn(T), 256);
   L.part_f = off;
@@ -106,6 +112,13 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap, bool split_ok = true
   L.total = off;
   return L;
 }
+
+// Host checks of int8_matmul's arguments (sizes, threshold, pointers, alignment) without a
+// workspace: I8_OK, or the status int8_matmul would return before launching anything.
+i8_status matmul_precheck(const void* X, int T, int in, const int8_t* CB, const float* SCB,
+                          int out, float threshold, const void* bias, const void* Y);
+// I8_OK if the current device is an sm_103 GPU (I8_ERR_UNSUPPORTED_DEVICE, I8_ERR_CUDA).
+i8_status current_device_check();
 
 // Smallest fp16 bit pattern whose value is >= threshold (0x7C00 = +inf if none is finite).
 uint16_t threshold_to_half_bits(float threshold);
@@ -165,7 +178,7 @@ struct GemmArgs {
   WsHeader* hdr = nullptr;      // status word + n_out (int8 path), may be null for fp16
   const float* rowabs = nullptr;
   const int32_t* l1 = nullptr;  // per (token tile, chunk) code-magnitude bounds, or null
-  int32_t* acc_scratch = nullptr;  // [kSmCount][BN][128] int32 epilogue running sums
+  int32_t* acc_scratch = nullptr;  // [sm_count()][BN][128] int32 epilogue running sums
   const float* scb = nullptr;
   const void* bias = nullptr;
   void* Y = nullptr;
