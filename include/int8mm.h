@@ -287,25 +287,36 @@ int i8_last_launch_count(void);
  * that runs where allocation is not allowed at all. The pages have no counterpart to this
  * call; it is a deployment convenience.
  *
- * Arguments, layouts, results and errors are those of int8_matmul minus the workspace.
+ * Arguments, layouts, results and errors are those of int8_matmul minus the workspace;
+ * arguments and the device are checked before the scratch is touched.
  * The scratch is a fixed array of I8_NOALLOC_SCRATCH_BYTES in device memory that every GPU
  * which loads this library reserves until the process exits. Sizes whose workspace (with a
  * 64-column outlier capacity) does not fit return I8_ERR_SCRATCH_LIMIT before any launch;
  * within the limit the outlier capacity is the largest multiple of 64 columns that fits.
- * Roughly: 2*T*in + 132*(T + out) + 4*in + 75776*BN bytes plus a few KB must fit in
- * 32 MiB, with BN the matmul's token tile (16, 32, 64, 128 or, above 128 tokens, 256).
- * - The first call on a device looks up the scratch's device address (once per device,
- *   with that device current); make that first call before any stream capture.
+ * Roughly: 2*T*in + 132*(T + out) + 4*in + 512*BN*SMs bytes plus a few KB must fit in
+ * 32 MiB, with BN the matmul's token tile (16, 32, 64, 128 or, above 128 tokens, 256) and
+ * SMs the device's multiprocessor count.
+ * - The first call on a device looks up the scratch's device address (once per device and
+ *   CUDA context, with that device current); make that first call before any stream
+ *   capture. After cudaDeviceReset the next call looks the address up again.
  * - All calls share the one scratch and it keeps the last call's contents; the parts that
  *   must start at zero are cleared by every call. Calls that overlap on the GPU (other
  *   streams, other host threads) race on the scratch: serialize them.
- * - The device status word lives in the scratch and is not readable through
- *   i8_get_status; more outlier columns than the capacity makes Y wrong silently.
+ * - Device-side errors (more outlier columns than the capacity, a wait that timed out) are
+ *   recorded in the scratch's status word: read them with i8_noalloc_status.
  * Calls no allocating routine.
  */
 i8_status int8_matmul_noalloc(const void* X, int T, int in, const int8_t* CB, const float* SCB,
                               int out, float threshold, const void* bias, void* Y,
                               void* stream);
+
+/*
+ * The device status word of the last int8_matmul_noalloc that launched work on the current
+ * device (I8_OK, I8_ERR_OUTLIER_CAP or I8_ERR_TIMEOUT; I8_OK before any such call), the
+ * counterpart of i8_get_status for the built-in scratch. Synchronizes `stream` first, so
+ * that the calls queued on it have finished. No counterpart in the pages.
+ */
+i8_status i8_noalloc_status(void* stream);
 
 /*
  * Profiling aid. `events` is NULL (off) or an array of 4 cudaEvent_t handles owned by the

@@ -28,6 +28,7 @@ SIGNATURES = {
     "int8_matmul_workspace_size": (_sz, [_i, _i, _i, _i]),
     "int8_matmul": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p, _sz, _p]),
     "int8_matmul_noalloc": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p]),
+    "i8_noalloc_status": (_i, [_p]),
     "int8_matmul_debug": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p, _sz, _p,
                                _p, _p, _p, _p, _p]),
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
@@ -97,6 +98,22 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _same_device(dev: torch.device, **tensors) -> None:
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, X on {dev}")
+
+
+def _out(Y: torch.Tensor | None, shape: tuple, dev: torch.device) -> torch.Tensor:
+    """The caller's output buffer after its checks, or a new one."""
+    if Y is None:
+        return torch.empty(shape, dtype=torch.float16, device=dev)
+    _need(Y, torch.float16, "Y")
+    if tuple(Y.shape) != tuple(shape):
+        raise ValueError(f"Y must have shape {tuple(shape)}, got {tuple(Y.shape)}")
+    return Y
+
+
 def int8_quantize_weight(W: torch.Tensor):
     """fp16 W [out, in] -> (CB int8 [out, in], SCB fp32 [out]) with W ~ CB*SCB/127."""
     _need(W, torch.float16, "W")
@@ -130,13 +147,14 @@ def int8_matmul(X: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, threshold:
     out = CB.shape[0]
     if bias is not None:
         _need(bias, torch.float16, "bias")
-    if Y is None:
-        Y = torch.empty((T, out), dtype=torch.float16, device=X.device)
+    Y = _out(Y, (T, out), X.device)
     if workspace is None:
         workspace = alloc_workspace(T, d, out, X.device)
-    _check("int8_matmul", lib().int8_matmul(
-        _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
-        _ptr(workspace), workspace.numel(), _stream(X.device)))
+    _same_device(X.device, CB=CB, SCB=SCB, bias=bias, Y=Y, workspace=workspace)
+    with torch.cuda.device(X.device):
+        _check("int8_matmul", lib().int8_matmul(
+            _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
+            _ptr(workspace), workspace.numel(), _stream(X.device)))
     return Y
 
 
@@ -144,18 +162,31 @@ def int8_matmul_noalloc(X: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor,
                         threshold: float = 6.0, bias: torch.Tensor | None = None,
                         Y: torch.Tensor | None = None) -> torch.Tensor:
     """int8_matmul on the library's built-in device scratch instead of a workspace, for
-    callers that cannot allocate device memory at call time (pass a preallocated Y)."""
+    callers that cannot allocate device memory at call time (pass a preallocated Y).
+    Device-side errors of the call are read with i8_noalloc_status(X.device)."""
     _need(X, torch.float16, "X")
     _need(CB, torch.int8, "CB")
     _need(SCB, torch.float32, "SCB")
+    if bias is not None:
+        _need(bias, torch.float16, "bias")
     T, d = X.shape
     out = CB.shape[0]
-    if Y is None:
-        Y = torch.empty((T, out), dtype=torch.float16, device=X.device)
-    _check("int8_matmul_noalloc", lib().int8_matmul_noalloc(
-        _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
-        _stream(X.device)))
+    Y = _out(Y, (T, out), X.device)
+    _same_device(X.device, CB=CB, SCB=SCB, bias=bias, Y=Y)
+    with torch.cuda.device(X.device):
+        _check("int8_matmul_noalloc", lib().int8_matmul_noalloc(
+            _ptr(X), T, d, _ptr(CB), _ptr(SCB), out, float(threshold), _ptr(bias), _ptr(Y),
+            _stream(X.device)))
     return Y
+
+
+def i8_noalloc_status(device=None) -> int:
+    """Synchronizes the device's current stream and returns the device status code of the
+    last int8_matmul_noalloc on it (0 = I8_OK)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().i8_noalloc_status(_stream(dev)))
 
 
 def int8_matmul_debug(X, CB, SCB, threshold=6.0, bias=None, workspace=None):

@@ -9,6 +9,26 @@
 #define I8_API extern "C" __attribute__((visibility("default")))
 
 namespace i8mm {
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {};  // 0: not looked up yet
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();  // no device here: leave no error pending for a later launch check
+    return kSmFallback;
+  }
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return kSmFallback;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 namespace {
 
 thread_local int g_last_launches = 0;
@@ -28,7 +48,10 @@ bool g_dev_init = false;
 
 i8_status check_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return I8_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();  // leave no error pending for a later launch check
+    return I8_ERR_CUDA;
+  }
   if (dev < 0 || dev >= 64) return I8_ERR_UNSUPPORTED_DEVICE;
   if (!g_dev_init) {
     for (int& v : g_dev_ok) v = -1;
@@ -37,8 +60,10 @@ i8_status check_device() {
   if (g_dev_ok[dev] < 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
       return I8_ERR_CUDA;
+    }
     g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 0;
   }
   return g_dev_ok[dev] ? I8_OK : I8_ERR_UNSUPPORTED_DEVICE;
@@ -383,6 +408,16 @@ i8_status run_ffn(const void* X, int T, int d_model, int d_ff, const int8_t* CB_
 }
 
 }  // namespace
+
+i8_status matmul_precheck(const void* X, int T, int in, const int8_t* CB, const float* SCB,
+                          int out, float threshold, const void* bias, const void* Y) {
+  // validate_matmul with a stand-in workspace pointer (aligned, never dereferenced)
+  const void* ws_stand_in = reinterpret_cast<const void*>(uintptr_t{256});
+  return validate_matmul(X, T, in, CB, SCB, out, threshold, bias, Y, ws_stand_in);
+}
+
+i8_status current_device_check() { return check_device(); }
+
 }  // namespace i8mm
 
 using namespace i8mm;
