@@ -60,8 +60,17 @@ def check_y(Y, ref):
                            f"{err.max():.4g} at ref {ref.flat[err.argmax()]:.4g}")
 
 
+def outlier_mask(idx, d):
+    m = np.zeros(d, np.uint8)
+    m[np.asarray(idx, np.int64)] = 1
+    return m
+
+
 def run_and_compare(i8, X, W, bias, threshold, rows=None, CBo=None, SCBo=None,
-                    check_weights=True):
+                    check_weights=True, all_codes=True):
+    """The CUDA path against the oracle: outlier set, codes and row absmax of every row
+    (all_codes) or of the evaluated rows, and the int32 products and Y of the evaluated
+    rows (all rows unless `rows` samples them)."""
     if CBo is None:
         CBo, SCBo = oracle.quantize_weight(W)
     Wd = dev(W)
@@ -76,9 +85,16 @@ def run_and_compare(i8, X, W, bias, threshold, rows=None, CBo=None, SCBo=None,
     rows = np.arange(T) if rows is None else rows
     ref = oracle.int8_matmul(X, CBo, SCBo, threshold=threshold, bias=bias, rows=rows)
     assert r["idx"].cpu().numpy().tolist() == ref["idx"].tolist(), "outlier set differs"
-    Xq = r["Xq"].cpu().numpy()[rows]
-    np.testing.assert_array_equal(Xq, ref["Q"])
-    np.testing.assert_array_equal(r["rowabs"].cpu().numpy()[rows], ref["rowabs"])
+    Xq_all = r["Xq"].cpu().numpy()
+    ra_all = r["rowabs"].cpu().numpy()
+    np.testing.assert_array_equal(Xq_all[rows], ref["Q"])
+    np.testing.assert_array_equal(ra_all[rows], ref["rowabs"])
+    if all_codes and len(rows) < T:
+        # every row's codes and row absmax, from the oracle's row quantizer over the
+        # inlier columns (the product is only evaluated on the sampled rows)
+        Qo, ao = oracle.quantize_rows_absmax(X, outlier_mask(ref["idx"], X.shape[1]))
+        np.testing.assert_array_equal(Xq_all, Qo)
+        np.testing.assert_array_equal(ra_all, ao)
     acc = r["acc"].cpu().numpy()[rows].astype(np.int64)
     np.testing.assert_array_equal(acc, ref["acc"])
     check_y(r["Y"].cpu().numpy()[rows], ref["Y"])
@@ -135,6 +151,28 @@ def test_no_bias_zero_row_and_all_outlier_row(i8):
     X[9, cols] = 50                                     # a row made only of outliers
     W[17] = 0                                           # zero weight row: SCB 0
     run_and_compare(i8, X, W, None, 6.0)
+
+
+@pytest.mark.parametrize("thr,below,at", [
+    (5.9, 5.8984375, 5.90234375),     # 5.9 lies between two fp16 values
+    (6.01, 6.0078125, 6.01171875),
+    (0.3, 0.2998046875, 0.30029296875),
+])
+def test_thresholds_that_are_not_fp16_values(i8, thr, below, at):
+    """A threshold between two fp16 values: the largest fp16 below it is an inlier, the
+    smallest above it an outlier (|x| >= threshold compared exactly). At 0.3 nearly every
+    column of N(0,1) data is an outlier and the inlier codes are mostly zero."""
+    w = synth.Workload("thr", 40, 256, 300, n_outlier_cols=2, seed=13)
+    X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
+    c0, c1 = np.setdiff1d(np.arange(256), synth.outlier_columns(w))[[20, 21]]
+    X[:, [c0, c1]] = np.clip(X[:, [c0, c1]], -0.1, 0.1)
+    X[3, c0] = below
+    X[7, c1] = -at
+    r, ref = run_and_compare(i8, X, W, bias, thr)
+    got = r["idx"].cpu().numpy().tolist()
+    assert c1 in got and c0 not in got
+    if thr < 1:
+        assert r["n_out"] == 255
 
 
 def test_threshold_inf_and_threshold_edge(i8):
@@ -247,11 +285,14 @@ def test_f16_matmul_comparator(i8, T, d, out):
 # ----------------------------------------------------------------- full-size configurations
 FULL = ["ffn_6.7b_up", "ffn_13b_up", "ffn_13b_down", "decode_176b_t1", "decode_176b_t8",
         "decode_176b_t64", "sweep_f0_thr6", "sweep_f0.1_thr6", "sweep_f0.5_thr6",
-        "sweep_f2_thr6", "sweep_f2_thrinf"]
+        "sweep_f2_thr6", "sweep_f0_thrinf", "sweep_f2_thrinf"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config_sampled_rows(i8, name):
+    """Every configuration at full size, in the launch configuration the benchmark times:
+    the outlier set, the codes and the row absmax of all T rows bit for bit; the int32
+    products and Y on sampled rows (the oracle's product of every row would take minutes)."""
     w = synth.WORKLOADS[name]
     X = synth.make_x(w)
     W, bias, (CBo, SCBo) = weights(w)

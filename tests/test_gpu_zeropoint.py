@@ -101,11 +101,22 @@ def test_threshold_inf_is_plain_vectorwise_zeropoint(i8):
     np.testing.assert_array_equal(ref["S"], Ss)
 
 
-def test_full_size_6p7b_sampled_rows(i8):
-    w = synth.WORKLOADS["ffn_6.7b_up"]
+@pytest.mark.parametrize("name", ["ffn_6.7b_up", "ffn_13b_up"])
+def test_full_size_sampled_rows(i8, name):
+    """Full size: codes, S and Z of every row bit for bit (the oracle's zeropoint row
+    quantizer over the inlier columns), the int32 products and Y on sampled rows."""
+    w = synth.WORKLOADS[name]
     rows = np.array(sorted({0, 1, 255, 256, 1024, w.T - 1, 777}), np.int64)
-    run_and_compare(i8, synth.make_x(w), synth.make_w(w), synth.make_bias(w), w.threshold,
-                    rows=rows)
+    X = synth.make_x(w)
+    r, ref = run_and_compare(i8, X, synth.make_w(w), synth.make_bias(w), w.threshold,
+                             rows=rows)
+    inl = np.setdiff1d(np.arange(w.d_in), ref["idx"])
+    Qo, So, Zo = oracle.zeropoint_rows(np.ascontiguousarray(X[:, inl]))
+    Q = r["Xq"].cpu().numpy()
+    np.testing.assert_array_equal(Q[:, inl], Qo)
+    assert not Q[:, ref["idx"]].any()
+    np.testing.assert_array_equal(r["S"].cpu().numpy(), So)
+    np.testing.assert_array_equal(r["Z"].cpu().numpy(), Zo)
 
 
 def test_rows_far_from_zero_take_the_64_bit_correction(i8):
