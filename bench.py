@@ -1,8 +1,9 @@
 """Benchmark of the LLM.int8() matmul (int8_matmul) on B300.
 
 One step = one int8_matmul over one batch: the column-statistics pass, the row quantize +
-outlier gather pass and the tensor-core matmul, on the FFN up-projection of a 6.7B-class
-model (X fp16 [2048, 4096] with 0.1% outlier columns, W [16384, 4096], threshold 6.0).
+outlier gather pass and the tensor-core matmul, on the FFN up-projection of a 13B-class
+model (X fp16 [4096, 5120] with 0.2% outlier columns, W [20480, 5120], threshold 6.0), the
+largest T x d -> 4d configuration that fits one GPU.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -36,7 +37,7 @@ import synth  # noqa: E402
 
 METRIC = "int8_matmul TOPS and % of INT8-tensor/HBM roofline on T×d→4d FFN GEMM"
 UNIT = "TOPS"
-DEFAULT_WORKLOAD = "ffn_6.7b_up"
+DEFAULT_WORKLOAD = "ffn_13b_up"
 ALL_CONFIGS = ["ffn_6.7b_up", "ffn_13b_up", "ffn_13b_down", "decode_176b_t1", "decode_176b_t8",
                "decode_176b_t64", "sweep_f0_thr6", "sweep_f0.1_thr6", "sweep_f0.5_thr6",
                "sweep_f2_thr6", "sweep_f0_thrinf", "sweep_f2_thrinf"]
