@@ -11,6 +11,9 @@ The zeropoint variant (``int8_matmul_zeropoint``) quantizes the activations' inl
 per row with S and Z (the zenn summary's "Zeropoint Quantization") instead of absmax and
 adds the correction Z * (sum of the inlier weight codes) to the exact integer product.
 
+Block-wise absmax (``quantize_blocks_absmax``) gives every block of ``block`` consecutive
+columns of a row its own absmax scale (the k-bit scaling review's small blocks of 64-128).
+
 The FFN block (``ffn``) chains two of these matmuls with ReLU (or nothing) between them,
 the intermediate rounded once from fp64 to fp16 as the second matmul's input.
 
@@ -44,6 +47,7 @@ def load(path: str) -> C.CDLL:
     L.orc_quantize_weight.argtypes = [p, i64, i64, p, p]
     L.orc_quantize_rows_absmax.argtypes = [p, i64, i64, p, p, p]
     L.orc_zeropoint_rows.argtypes = [p, i64, i64, p, p, p]
+    L.orc_quantize_blocks_absmax.argtypes = [p, i64, i64, i64, p, p]
     L.orc_outlier_weights.argtypes = [p, p, i64, i64, p, C.c_int32, p]
     L.orc_int8_matmul.argtypes = [p, i64, i64, p, p, i64, C.c_float, p, p, i64, p, p, p,
                                   p, p, C.c_int]
@@ -119,6 +123,21 @@ def quantize_rows_absmax(X: np.ndarray, outlier_mask: np.ndarray | None = None):
     Q = np.empty((rows, cols), np.int8)
     a = np.empty(rows, np.float32)
     lib().orc_quantize_rows_absmax(_ptr(X), rows, cols, _ptr(m), _ptr(Q), _ptr(a))
+    return Q, a
+
+
+def quantize_blocks_absmax(X: np.ndarray, block: int):
+    """(Q int8 [rows,cols], absmax float32 [rows, ceil(cols/block)]): each row cut into
+    blocks of `block` columns (the last one shorter if block does not divide cols), each
+    block quantized with its own absmax."""
+    X = _f16(X)
+    rows, cols = X.shape
+    if block <= 0:
+        raise ValueError("block must be positive")
+    nb = (cols + block - 1) // block
+    Q = np.empty((rows, cols), np.int8)
+    a = np.empty((rows, nb), np.float32)
+    lib().orc_quantize_blocks_absmax(_ptr(X), rows, cols, block, _ptr(Q), _ptr(a))
     return Q, a
 
 

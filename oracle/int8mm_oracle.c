@@ -124,6 +124,32 @@ void orc_quantize_rows_absmax(const uint16_t* X, int64_t rows, int64_t cols,
   }
 }
 
+/* Block-wise absmax quantization ("[論文レビュー] The case for 4-bit precision: k-bit
+ * Inference Scaling Laws" (nubint review), sections "提案手法" and "主な発見": the block size
+ * is a parameter of the quantizer, small blocks of 64-128 values each with their own
+ * normalization). Reading: each row of X [rows, cols] is cut into blocks of `block`
+ * consecutive columns, the last block of a row shorter when block does not divide cols;
+ * block k of row i holds absmax[i * nblocks + k] = max |x| over its columns and the codes
+ * clamp(rint(x * (127/absmax))) as in the row-wise quantizer (absmax 0: codes 0). */
+void orc_quantize_blocks_absmax(const uint16_t* X, int64_t rows, int64_t cols, int64_t block,
+                                int8_t* Q, float* absmax) {
+  const int64_t nblocks = (cols + block - 1) / block;
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t k = 0; k < nblocks; ++k) {
+      const int64_t j0 = k * block;
+      const int64_t j1 = (j0 + block < cols) ? j0 + block : cols;
+      float a = 0.0f;
+      for (int64_t j = j0; j < j1; ++j) {
+        float v = fabsf(h2f(X[i * cols + j]));
+        if (v > a) a = v;
+      }
+      absmax[i * nblocks + k] = a;
+      float s = absmax_scale(a);
+      for (int64_t j = j0; j < j1; ++j) Q[i * cols + j] = absmax_code(h2f(X[i * cols + j]), s);
+    }
+  }
+}
+
 /* Zeropoint (asymmetric) quantization of one row, X8 = INT8(X*S - Z) with
  * S = 254/(max-min) and Z = rint(S*min) + 127, so that min maps to -127, max to +127 and 0
  * to the integer -Z. min and max are taken over the columns not flagged in `outlier`

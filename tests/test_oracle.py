@@ -262,6 +262,89 @@ def test_zeropoint_zero_maps_exactly_and_constant_row():
     assert (rec[1] == 2.5).all()
 
 
+# --------------------------------------------------------------------------- block-wise absmax
+def power_of_two_blocks(rows, cols, block, seed):
+    """X whose block k of row i is c * 2^e with integers c in [-127, 127], one |c| = 127 per
+    block and a different exponent e per block: every block scale 127/(127 * 2^e) = 2^-e is
+    exact in fp32, so the codes are exactly c and the absmax exactly 127 * 2^e."""
+    g = np.random.default_rng(seed)
+    nb = (cols + block - 1) // block
+    C = g.integers(-127, 128, (rows, cols))
+    E = g.integers(-10, 4, (rows, nb))
+    for i in range(rows):
+        for k in range(nb):
+            j0 = k * block
+            C[i, j0 + g.integers(0, min(block, cols - j0))] = 127 * g.choice([-1, 1])
+    X = (C * np.exp2(np.repeat(E, block, axis=1)[:, :cols])).astype(np.float16)
+    assert np.array_equal(X.astype(np.float64), C * np.exp2(np.repeat(E, block, 1)[:, :cols]))
+    return X, C, 127.0 * np.exp2(E)
+
+
+@pytest.mark.parametrize("block,cols", [(64, 256), (128, 1024), (64, 3 * 64 + 20), (128, 100)])
+def test_blockwise_power_of_two_blocks_are_exact(block, cols):
+    """Each block has its own scale: the codes are the integers c of every block, including a
+    shorter last block, and the stored absmax is each block's own (a row-wide absmax would
+    shrink the codes of the blocks with smaller exponents)."""
+    X, C, A = power_of_two_blocks(5, cols, block, seed=block + cols)
+    Q, a = oracle.quantize_blocks_absmax(X, block)
+    assert a.shape == A.shape
+    assert np.array_equal(a.astype(np.float64), A)
+    assert np.array_equal(Q.astype(np.int64), C)
+
+
+def test_blockwise_page_example_as_one_block():
+    """The pages' worked absmax vector as block 1 of a row of 4-value blocks, between blocks
+    of much larger and much smaller values: its codes are the page's, whatever its
+    neighbours hold."""
+    g = json.load(open(os.path.join(GOLDEN, "absmax_worked_example.json")))
+    v = g["vector_printed"]
+    X = np.array([[100.0, -3.0, 7.0, 50.0] + v + [0.01, -0.02, 0.005, 0.0]], np.float16)
+    Q, a = oracle.quantize_blocks_absmax(X, 4)
+    assert Q[0, 4:8].tolist() == [28, -12, -101, 127]
+    assert a[0, 1] == np.float32(np.float16(g["absmax_printed"]))
+    assert Q[0, 0] == 127 and Q[0, 9] == -127
+
+
+def test_blockwise_with_one_block_per_row_is_the_row_quantizer():
+    X = synth.make_random_f16(77, (9, 300), std=1.3)
+    X[2] = 0
+    Qr, ar = oracle.quantize_rows_absmax(X)
+    for block in (300, 512):
+        Qb, ab = oracle.quantize_blocks_absmax(X, block)
+        assert np.array_equal(Qb, Qr) and np.array_equal(ab[:, 0], ar)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_blockwise_half_step_bound_range_and_independence(block):
+    """Per block: |x - q*a/127| <= a/254 (up to fp32 rounding of the scale and product),
+    codes in [-127, 127], the largest |code| of a non-zero block is 127, a zero block codes
+    to 0; changing one block changes no other block's codes or absmax."""
+    g = np.random.default_rng(block)
+    rows, cols = 6, 8 * block + 40
+    nb = (cols + block - 1) // block
+    scales = np.exp2(g.integers(-6, 6, (rows, nb)))
+    X = (g.standard_normal((rows, cols)) * np.repeat(scales, block, 1)[:, :cols]).astype(np.float16)
+    X[1, block:2 * block] = 0
+    Q, a = oracle.quantize_blocks_absmax(X, block)
+    x = X.astype(np.float64)
+    af = np.repeat(a.astype(np.float64), block, 1)[:, :cols]
+    err = np.abs(x - Q.astype(np.float64) * af / 127.0)
+    assert (err <= af / 254.0 * (1 + 2e-6) + 1e-12).all()
+    assert Q.min() >= -127 and Q.max() <= 127
+    for i in range(rows):
+        for k in range(nb):
+            q = Q[i, k * block:(k + 1) * block]
+            assert (np.abs(q).max() == 127) == (a[i, k] > 0)
+    assert a[1, 1] == 0 and not Q[1, block:2 * block].any()
+    X2 = X.copy()
+    X2[3, 2 * block:3 * block] *= np.float16(4)
+    Q2, a2 = oracle.quantize_blocks_absmax(X2, block)
+    other = np.ones(cols, bool)
+    other[2 * block:3 * block] = False
+    assert np.array_equal(Q2[:, other], Q[:, other]) and np.array_equal(Q2[:3], Q[:3])
+    assert a2[3, 2] == 4 * a[3, 2] and np.array_equal(np.delete(a2, 2, 1), np.delete(a, 2, 1))
+
+
 # --------------------------------------------------------------------------- FFN block
 @pytest.mark.parametrize("outliers", [False, True])
 def test_integer_ffn_block_reduces_to_exact_integer_chain(outliers):

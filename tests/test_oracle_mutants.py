@@ -36,6 +36,14 @@ MUTANTS = [
      "cbin[o] += CB[o * in + j];"),
     ("zeropoint scale inverted", "/ (127.0 * (double)jb->rowS[r])",
      "* (double)jb->rowS[r] / 127.0"),
+    ("block absmax over the whole row",
+     "for (int64_t j = j0; j < j1; ++j) {\n        float v = fabsf(h2f(X[i * cols + j]));",
+     "for (int64_t j = 0; j < cols; ++j) {\n        float v = fabsf(h2f(X[i * cols + j]));"),
+    ("block one column short", "(j0 + block < cols) ? j0 + block : cols",
+     "(j0 + block - 1 < cols) ? j0 + block - 1 : cols"),
+    ("block absmax stored transposed", "absmax[i * nblocks + k] = a;", "absmax[k * rows + i] = a;"),
+    ("ragged last block dropped", "const int64_t nblocks = (cols + block - 1) / block;",
+     "const int64_t nblocks = cols / block;"),
     ("zeropoint range over outlier columns",
      "if (outlier && outlier[j]) continue;\n    float v = h2f(x[j]);",
      ";\n    float v = h2f(x[j]);"),
@@ -57,6 +65,10 @@ PIN_TESTS = [
     lambda: pins.test_zeropoint_matmul_on_one_sided_grid_rows_is_exact(True),
     pins.test_zeropoint_matmul_constant_and_all_outlier_rows,
     pins.test_zeropoint_matmul_within_quantization_error_bound,
+    lambda: pins.test_blockwise_power_of_two_blocks_are_exact(64, 3 * 64 + 20),
+    pins.test_blockwise_page_example_as_one_block,
+    pins.test_blockwise_with_one_block_per_row_is_the_row_quantizer,
+    lambda: pins.test_blockwise_half_step_bound_range_and_independence(64),
 ]
 
 
