@@ -131,6 +131,22 @@ i8_status absmax_quantize_rows(const void* X, int rows, int cols, int8_t* Q, flo
                                void* stream);
 
 /*
+ * Block-wise absmax quantization ("[論文レビュー] The case for 4-bit precision: k-bit Inference
+ * Scaling Laws" (nubint review), sections "提案手法" and "主な発見": small blocks of 64-128
+ * values, each with its own absmax scale). Each row is cut into blocks of `block`
+ * consecutive columns (the last block of a row is shorter when block does not divide
+ * cols); each block is quantized as absmax_quantize_rows quantizes a row.
+ *   X      : fp16 [rows, cols]                    input
+ *   block  : values per block (> 0); block >= cols gives absmax_quantize_rows' result
+ *   Q      : int8 [rows, cols]                    codes rint(x * 127/absmax of the block)
+ *   absmax : fp32 [rows, ceil(cols / block)]     per-block max |x| (0: codes 0)
+ * rows == 0 or cols == 0 is a no-op. One kernel launch; it streams X at HBM rate when
+ * cols % 8 == 0 and block is 16, 32, 64, 128 or 256, element by element otherwise.
+ */
+i8_status absmax_quantize_blocks(const void* X, int rows, int cols, int block, int8_t* Q,
+                                 float* absmax, void* stream);
+
+/*
  * Row-wise zeropoint quantization ("Zeropoint Quantization": X8 = INT8(X*S - Z),
  * S = 254/(max - min)). Z = rint(S*min) + 127 is an integer so that 0 maps to an exact
  * code; dequantize with X ~ (Q + Z)/S. A constant row stores S = 0, Z = min, codes 0.

@@ -32,6 +32,7 @@ SIGNATURES = {
     "int8_matmul_debug": (_i, [_p, _i, _i, _p, _p, _i, _f, _p, _p, _p, _sz, _p,
                                _p, _p, _p, _p, _p]),
     "absmax_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p]),
+    "absmax_quantize_blocks": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "zeropoint_quantize_rows": (_i, [_p, _i, _i, _p, _p, _p, _p]),
     "f16_matmul": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
     "int8_weight_code_sums": (_i, [_p, _i, _i, _p, _p]),
@@ -221,6 +222,22 @@ def absmax_quantize_rows(X: torch.Tensor):
     a = torch.empty(rows, dtype=torch.float32, device=X.device)
     _check("absmax_quantize_rows", lib().absmax_quantize_rows(
         _ptr(X), rows, cols, _ptr(Q), _ptr(a), _stream(X.device)))
+    return Q, a
+
+
+def absmax_quantize_blocks(X: torch.Tensor, block: int = 64):
+    """fp16 X [rows, cols] -> (int8 Q, fp32 absmax [rows, ceil(cols / block)]): each block of
+    `block` consecutive columns of a row quantized with its own absmax."""
+    _need(X, torch.float16, "X")
+    if block <= 0:
+        raise ValueError("block must be positive")
+    rows, cols = X.shape
+    nb = (cols + block - 1) // block
+    Q = torch.empty((rows, cols), dtype=torch.int8, device=X.device)
+    a = torch.empty((rows, nb), dtype=torch.float32, device=X.device)
+    with torch.cuda.device(X.device):
+        _check("absmax_quantize_blocks", lib().absmax_quantize_blocks(
+            _ptr(X), rows, cols, int(block), _ptr(Q), _ptr(a), _stream(X.device)))
     return Q, a
 
 

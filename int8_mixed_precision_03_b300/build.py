@@ -13,7 +13,7 @@ LIB = os.path.join(HERE, "libint8mm.so")
 ROOT = os.path.dirname(HERE)
 
 SOURCES = ["capi.cu", "colstats.cu", "quantize.cu", "gemm_i8.cu", "gemm_f16.cu", "gemv_i8.cu",
-           "gemv_mma.cu", "noalloc.cu"]
+           "gemv_mma.cu", "noalloc.cu", "blocks.cu"]
 HEADERS = ["int8mm_internal.h", "sm103_ptx.cuh", "gemm_common.cuh", os.path.join("..", "..", "include", "int8mm.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -148,7 +148,7 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
     int8_t* xq8 = reinterpret_cast<int8_t*>(ws + L.xq);
     if ((st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
                                                mask, idx, ncap, nullptr, rowabs, ws + L.xout,
-                                               nullptr, l1, xq8, s))) != I8_OK)
+                                               nullptr, nullptr, l1, xq8, s))) != I8_OK)
       return st;
     ++g_last_launches;
     if (ly.prof_base >= 0) prof_mark(ly.prof_base + 2, s);
@@ -180,12 +180,12 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
     if (zp)
       st = from_cuda(launch_quantize_gather_zp(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
                                                mask, idx, ncap, ws + L.xq, rowabs, zi,
-                                               ws + L.xout, ws + L.wout, cbout, l1, ly.dbg_xq,
-                                               ly.dbg_S, ly.dbg_Z, s));
+                                               ws + L.xout, ws + L.wout, ws + L.xoT, cbout, l1,
+                                               ly.dbg_xq, ly.dbg_S, ly.dbg_Z, s));
     else
       st = from_cuda(launch_quantize_gather(ly.X, ly.T, ly.in, ly.CB, ly.SCB, ly.out, hdr,
                                             mask, idx, ncap, ws + L.xq, rowabs, ws + L.xout,
-                                            ws + L.wout, l1, ly.dbg_xq, s));
+                                            ws + L.wout, ws + L.xoT, l1, ly.dbg_xq, s));
     if (st != I8_OK) return st;
     ++g_last_launches;
     if (ly.prof_base >= 0) prof_mark(ly.prof_base + 2, s);
@@ -194,6 +194,7 @@ i8_status launch_layer(const Layer& ly, cudaStream_t s) {
     g.b_f16 = ws + L.xq;
     g.wout = ws + L.wout;
     g.xout = ws + L.xout;
+    g.xoT = ws + L.xoT;
     g.ncap = ncap;
     g.hdr = hdr;
     g.rowabs = rowabs;
@@ -533,6 +534,20 @@ I8_API i8_status absmax_quantize_rows(const void* X, int rows, int cols, int8_t*
   i8_status st = check_device();
   if (st != I8_OK) return st;
   st = from_cuda(launch_absmax_rows(X, rows, cols, Q, absmax, static_cast<cudaStream_t>(stream)));
+  if (st == I8_OK) g_last_launches = 1;
+  return st;
+}
+
+I8_API i8_status absmax_quantize_blocks(const void* X, int rows, int cols, int block, int8_t* Q,
+                                        float* absmax, void* stream) {
+  g_last_launches = 0;
+  if (rows < 0 || cols < 0 || block <= 0 || !X || !Q || !absmax) return I8_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q) || !aligned16(absmax)) return I8_ERR_ALIGNMENT;
+  if (rows == 0 || cols == 0) return I8_OK;
+  i8_status st = check_device();
+  if (st != I8_OK) return st;
+  st = from_cuda(launch_absmax_blocks(X, rows, cols, block, Q, absmax,
+                                      static_cast<cudaStream_t>(stream)));
   if (st == I8_OK) g_last_launches = 1;
   return st;
 }

@@ -123,11 +123,13 @@ __device__ __forceinline__ void box_reuse_wait(int lane) {
 // Writes this lane's kW outputs (one feature, kW tokens; fp16 pairs in yh) into its box
 // column and stores the box to Y[tok0 .. +kW, feat0 .. +32]. With a Y tensor map (Y's row
 // pitch a multiple of 16 bytes) that is one TMA store, clipped by the map at the edges of
-// Y; without one the lanes copy the box out element by element.
+// Y, whose lines are marked first to leave L2 (`policy`: Y is not read again here, and the
+// operands the matmul re-reads across waves should stay); without one the lanes copy the
+// box out element by element.
 template <int kW>
 __device__ __forceinline__ void box_store(uint8_t* box, const uint32_t (&yh)[kW / 2],
                                           const CUtensorMap* mapY, uint16_t* Y, int T, int out,
-                                          int feat0, int tok0, int lane) {
+                                          int feat0, int tok0, int lane, uint64_t policy) {
   const uint32_t b = smem_u32(box);
 #pragma unroll
   for (int j = 0; j < kW; ++j) {
@@ -138,7 +140,7 @@ __device__ __forceinline__ void box_store(uint8_t* box, const uint32_t (&yh)[kW 
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(mapY, box, feat0, tok0);
+      tma_store_2d_hint(mapY, box, feat0, tok0, policy);
       bulk_commit_group();
     }
   } else {

@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     if (lane == 0) {
+      // X (the B operand) is re-read by every weight strip: keep it in L2 across waves
+      const uint64_t keep = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
           mbar_arrive_expect_tx(&full[s], kA16Bytes + C::kBBytes);
           tma_load_2d(smem + C::a + s * kA16Bytes, &tmA, &full[s], kb * BK, m0);
-          tma_load_2d(smem + C::b + s * C::kBBytes, &tmB, &full[s], kb * BK, n0);
+          tma_load_2d_hint(smem + C::b + s * C::kBBytes, &tmB, &full[s], kb * BK, n0, keep);
         }
       }
       for (uint32_t k = 0; k < (uint32_t)kStages && k < it; ++k) {
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
     uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
     const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+    const uint64_t y_policy = l2_policy_evict_first();
     uint32_t nt = 0, slot = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++nt) {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         box_reuse_wait(lane);
         box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
-                      n0 + j0, lane);
+                      n0 + j0, lane, y_policy);
         slot ^= 1u;
       }
       tc_fence_before();

@@ -26,12 +26,21 @@
 //       slice X_out fp16 [T, ncap]: TMA, 128-byte swizzle, K-major.
 //   A and B stages form one ring, released by one MMA commit per K block.
 // TMEM: two accumulators F0 [0, BN) and F1 [BN, 2BN) take the segments in turn (the int
-// segments of a tile, then its outlier segment, then the next tile's), so the epilogue of
-// one segment overlaps the MMAs of the next. The epilogue's running int32 sum of a tile
-// lives in a per-CTA slot of the workspace (L2 resident): a segment that is not the last
-// of its tile is folded into it, and the tile's last segment reads it back.
+// segments of a tile, then its outlier segment if it has one, then the next tile's), so the
+// epilogue of one segment overlaps the MMAs of the next. The epilogue's running int32 sum of
+// a tile lives in a per-CTA slot of the workspace (L2 resident): a segment that is not the
+// last of its tile is folded into it, and the tile's last segment reads it back.
+// Outlier product: with at most kCcOut outlier columns (the usual case: about 0.1% of the
+// hidden dimensions) the epilogue computes it on the CUDA cores, sum_k X_out[t,k] W_out[o,k]
+// in fp32 from a token-contiguous transposed copy of X_out (one broadcast load per column
+// and 16 tokens) and this feature's W_out row held in registers. A tile then has no short
+// outlier segment after its long int segment, so the next tile's MMAs never wait for the
+// epilogue to drain the int accumulator. With more outlier columns they run as the tile's
+// last MMA segment (fp16 operands, fp32 accumulation in TMEM) of ceil(n/64) K blocks.
 // Epilogue: Y[t, o] = fp16(acc * rowabs[t] * SCB[o] / 127^2 + outlier + bias[o]), staged
 // per warp in shared memory (two boxes of tokens x 32 features) and written by TMA stores.
+// L2 policy: the activation codes, re-read by every weight strip, are loaded evict-last,
+// and Y, written once, is stored evict-first, so that the codes stay in L2 across waves.
 // With zeropoint activation codes (x ~ (q + Z)/S per token, "LLM.int8() summary" (zenn),
 // "Zeropoint Quantization") the epilogue adds Z_t times the feature's code sum over the
 // inlier columns to the exact int32 product, in 64-bit integers, before scaling by
@@ -62,6 +71,13 @@ constexpr int kThreads = 512;
 constexpr int kWarpB = 0, kWarpMma = 1, kWarpA8 = 2;
 constexpr int kWarpConv0 = 4, kWarpEpi0 = 8, kWarpConv1 = 12;
 constexpr uint32_t kExactLimit = 1u << 24;                    // integers exact in fp32
+// Up to this many outlier columns the epilogue adds the outlier product on the CUDA cores;
+// beyond it the outlier product runs as the tile's last MMA segment (see the file comment).
+constexpr int kCcOut = kCcOutlierCols;
+static_assert(kCcOut == 32, "one transposed X_out row per lane");
+// Largest outlier count sent to the CUDA-core path (<= kCcOut): above it the outlier
+// product is cheaper as an MMA segment than as per-element work in the epilogue.
+constexpr int kCcMaxDefault = 32;
 constexpr uint32_t kWorstChunkBound = 127u * 127u * kChunkK;  // < kExactLimit
 static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact");
 
@@ -117,6 +133,13 @@ struct Params {
   int32_t* part;              // [G][2][BN][128] int32: a CTA's first / last piece's sums
   float* part_f;              // [G][BN][128] fp32: outlier sums of a tile-ending piece
   int32_t* tile_cnt;          // [tiles] arrivals, zeroed per call
+  // outlier product on the CUDA cores (0 < n_out <= kCcOut): W_out [out, ncap] and X_out
+  // transposed, xoT [kCcOut][xo_stride] (token-contiguous rows, zeros past n_out)
+  const uint16_t* wout;
+  int ncap;
+  const uint16_t* xoT;
+  int xo_stride;
+  int cc_max;                 // outlier counts 1 .. cc_max take the CUDA-core path
   uint64_t timeout_ns;
   int debug_skip_loads;
 };
@@ -166,9 +189,92 @@ __device__ __forceinline__ int unit_owner(const Params& p, long long u) {
 // zeropoint codes (acc + zi[t] * inlier code sum of feature o), the same + int32 export.
 enum EpiMode { kEpiPlain = 0, kEpiDebug = 1, kEpiNext = 2, kEpiZp = 3, kEpiZpDebug = 4 };
 
-__device__ __forceinline__ int outlier_kblocks(const Params& p) {
-  const int n = *reinterpret_cast<volatile const int*>(&p.hdr->n_out_used);
-  return (n + 63) / 64;
+__device__ __forceinline__ int outlier_count(const Params& p) {
+  return *reinterpret_cast<volatile const int*>(&p.hdr->n_out_used);
+}
+// The outlier columns are multiplied on the CUDA cores in the epilogue when there are at
+// most kCcOut of them (and the transposed slice was written); otherwise, and in every role
+// alike, they form the tile's last MMA segment of ceil(n/64) K blocks.
+__device__ __forceinline__ bool cc_outliers(const Params& p, int n) {
+  return p.xoT != nullptr && n > 0 && n <= p.cc_max;
+}
+
+// This lane's outlier weights W_out[o, 0 .. kCcOut) as fp16 pairs (W_out is zero past the
+// outlier count; a feature beyond `out` gets zeros).
+__device__ __forceinline__ void load_cc_weights(const Params& p, int o, bool o_ok, int n,
+                                                uint32_t (&wh)[kCcOut / 2]) {
+#pragma unroll
+  for (int c = 0; c < kCcOut / 8; ++c) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (o_ok && 8 * c < n) v = __ldg(reinterpret_cast<const uint4*>(p.wout + (size_t)o * p.ncap) + c);
+    wh[4 * c + 0] = v.x;
+    wh[4 * c + 1] = v.y;
+    wh[4 * c + 2] = v.z;
+    wh[4 * c + 3] = v.w;
+  }
+}
+
+// lo += x.lo * w, hi += x.hi * w for the two fp16 values of x (low and high half) and the
+// fp16 weight in half `wsel` of w2: fp16 products are exact in fp32 and each sum is rounded
+// once, as fmaf on the converted values would.
+__device__ __forceinline__ void fma2_f16_f32(float& lo, float& hi, uint32_t x, uint32_t w2,
+                                             int wsel) {
+  if (wsel)
+    asm("{\n.reg .f16 xl, xh, wl, wh;\n"
+        "mov.b32 {xl, xh}, %2;\n"
+        "mov.b32 {wl, wh}, %3;\n"
+        "fma.rn.f32.f16 %0, xl, wh, %0;\n"
+        "fma.rn.f32.f16 %1, xh, wh, %1;\n}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(x), "r"(w2));
+  else
+    asm("{\n.reg .f16 xl, xh, wl, wh;\n"
+        "mov.b32 {xl, xh}, %2;\n"
+        "mov.b32 {wl, wh}, %3;\n"
+        "fma.rn.f32.f16 %0, xl, wl, %0;\n"
+        "fma.rn.f32.f16 %1, xh, wl, %1;\n}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(x), "r"(w2));
+}
+
+// The transposed X_out rows of a slice of 16 tokens tok0 .. tok0 + 15: lane k loads row k
+// (outlier column k, 32 bytes), so one coalesced load per lane brings the whole slice; rows
+// k >= n and slices past the last token are zero.
+__device__ __forceinline__ void cc_load_rows(const Params& p, int tok0, int n, int lane,
+                                             uint4& a, uint4& b) {
+  a = make_uint4(0u, 0u, 0u, 0u);
+  b = a;
+  if (lane < n && tok0 < p.T) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.xoT + (size_t)lane * p.xo_stride + tok0);
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+}
+
+// Outlier product of the 16 tokens of a slice for this lane's feature:
+// fo[j] = sum_{k < n} X_out[tok0 + j, k] * W_out[o, k], fp32 fused multiply-adds in
+// ascending k, so every schedule gives the same bits. Row k of the slice (loaded by lane k
+// with cc_load_rows) reaches every lane by shuffles; rows n .. are zero, so steps of four
+// columns need no mask (n is the same for the whole warp).
+__device__ __forceinline__ void cc_outlier_slice(int n, const uint32_t (&wh)[kCcOut / 2],
+                                                 const uint4& a, const uint4& b,
+                                                 float (&fo)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) fo[j] = 0.0f;
+#pragma unroll
+  for (int k0 = 0; k0 < kCcOut; k0 += 4) {
+    if (k0 >= n) break;
+#pragma unroll
+    for (int k = k0; k < k0 + 4; ++k) {
+      const uint32_t w2 = wh[k >> 1];
+      const uint32_t xw[8] = {__shfl_sync(0xffffffffu, a.x, k), __shfl_sync(0xffffffffu, a.y, k),
+                              __shfl_sync(0xffffffffu, a.z, k), __shfl_sync(0xffffffffu, a.w, k),
+                              __shfl_sync(0xffffffffu, b.x, k), __shfl_sync(0xffffffffu, b.y, k),
+                              __shfl_sync(0xffffffffu, b.z, k), __shfl_sync(0xffffffffu, b.w, k)};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) fma2_f16_f32(fo[2 * e], fo[2 * e + 1], xw[e], w2, k & 1);
+    }
+  }
 }
 
 // Bound on |partial sums| of chunk c for token tile n_blk (see the file comment).
@@ -263,13 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_base_smem;
 
   const int tiles = p.m_tiles * p.n_tiles;
-  const int nkb_out = outlier_kblocks(p);
+  // outlier columns: on the CUDA cores in the epilogue (n_cc of them), or as the tile's last
+  // MMA segment (nkb_out K blocks); every role takes the same decision
+  const int n_out_all = outlier_count(p);
+  const bool cc = cc_outliers(p, n_out_all);
+  const int n_cc = cc ? n_out_all : 0;
+  const int nkb_out = cc ? 0 : (n_out_all + 63) / 64;
   const int nkb_all = p.nkb + nkb_out;
   const uint32_t sbase = smem_u32(smem);
 
   if (warp == kWarpB) {
     // -------------------------------------------------------- TMA: B operand
     if (lane == 0 && !p.debug_skip_loads) {
+      // the activation codes are re-read by every weight strip: keep them in L2 across waves
+      const uint64_t keep = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
       Sched<kSplit> sc(p);
@@ -282,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
           mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
           if (kb < p.nkb)
-            tma_load_2d(smem + C::b + s * C::kBBytes, &tmB, &full_b[s], kb * BK, n0);
+            tma_load_2d_hint(smem + C::b + s * C::kBBytes, &tmB, &full_b[s], kb * BK, n0, keep);
           else
             tma_load_2d(smem + C::b + s * C::kBBytes, &tmXo, &full_b[s], (kb - p.nkb) * BK, n0);
         }
@@ -463,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
       uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
       const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+      const uint64_t y_policy = l2_policy_evict_first();
       // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
       int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
       uint32_t nseg = 0, slot = 0;
@@ -485,6 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // zeropoint: sum of this feature's codes over the inlier columns
         [[maybe_unused]] const int cbin =
             (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
+        uint32_t wh[kCcOut / 2];  // this feature's outlier weights (CUDA-core outlier product)
+        load_cc_weights(p, o, o_ok, n_cc, wh);
         const int nseg_int = count_int_segments(p, n_blk, 0, p.nchunks);
         const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
         uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
@@ -501,6 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           int pn[kW];
   #pragma unroll
           for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
+          static_assert(kW == 16, "CUDA-core outlier slices are 16 tokens");
+          uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;  // the slice's transposed X_out
+          if (last) cc_load_rows(p, n0, n_cc, lane, xa, xb);  // rows (CUDA-core outliers)
           if (!last) {
             // an int segment that is not the last one of the tile: fold it into the
             // running sum (first segment: store it)
@@ -534,6 +653,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
                 for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
               }
+              uint4 na, nb;  // the next slice's rows, loaded while this one is computed
+              cc_load_rows(p, n0 + j0 + kW < n0 + BN ? n0 + j0 + kW : p.T, n_cc, lane, na, nb);
+              float fcc[kW];  // outlier product of this slice (zeros unless cc)
+              cc_outlier_slice(n_cc, wh, xa, xb, fcc);
+              xa = na;
+              xb = nb;
               uint32_t f[kW];
               tmem_ld<kW>(tF + j0, f);
               tmem_ld_wait();
@@ -548,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
               for (int j = 0; j < kW; ++j) {
                 int acc;
-                float fo = 0.0f;
+                float fo = fcc[j];
                 if (is_out) {
                   acc = pc[j];
                   fo = __uint_as_float(f[j]);
@@ -583,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               box_reuse_wait(lane);
               box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
-                            n0 + j0, lane);
+                            n0 + j0, lane, y_policy);
               slot ^= 1u;
               if constexpr (kDebug) {
   #pragma unroll 1
@@ -616,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
       uint8_t* boxes = smem + C::box + q * 2 * C::kBoxBytes;
       const CUtensorMap* mapY = p.y_tma ? &tmY : nullptr;
+      const uint64_t y_policy = l2_policy_evict_first();
       volatile int* s_fin = reinterpret_cast<volatile int*>(smem + C::misc + 8);
       // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
       int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
@@ -649,6 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // zeropoint: sum of this feature's codes over the inlier columns
         [[maybe_unused]] const int cbin =
             (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
+        uint32_t wh[kCcOut / 2];  // this feature's outlier weights (CUDA-core outlier product)
+        load_cc_weights(p, o, o_ok, n_cc, wh);
         const bool has_out = c1 == p.nchunks && nkb_out > 0;
         const int nseg_int = count_int_segments(p, n_blk, c0, c1);
         const int nseg_tile = nseg_int + (has_out ? 1 : 0);
@@ -668,10 +796,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto emit = [&](int j0, const int (&accv)[kW], const float (&fov)[kW]) {
           const float ra_s = ra[0];  // this slice's tokens, one per lane
           [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
+          uint4 xa, xb;
+          cc_load_rows(p, n0 + j0, n_cc, lane, xa, xb);
+          float fcc[kW];  // outlier product of this slice (zeros unless cc)
+          cc_outlier_slice(n_cc, wh, xa, xb, fcc);
           uint32_t yh[kW / 2];
   #pragma unroll
           for (int j = 0; j < kW; ++j) {
             const int acc = accv[j];
+            const float fo = fov[j] + fcc[j];
             const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
             float y;
             if constexpr (kZp) {
@@ -680,13 +813,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               // so the branch is uniform), in 64 bits otherwise
               const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
               if (abs(zj) <= p.z_safe) {
-                y = (float)(acc + zj * cbin) * (rj * so) + fov[j] + bo;
+                y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
               } else {
                 const long long az = (long long)acc + (long long)zj * (long long)cbin;
-                y = __ll2float_rn(az) * (rj * so) + fov[j] + bo;
+                y = __ll2float_rn(az) * (rj * so) + fo + bo;
               }
             } else {
-              y = (float)acc * (rj * so) + fov[j] + bo;
+              y = (float)acc * (rj * so) + fo + bo;
             }
             if constexpr (kNext) {
               if (p.next_relu) y = fmaxf(y, 0.0f);
@@ -699,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           box_reuse_wait(lane);
           box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
-                        n0 + j0, lane);
+                        n0 + j0, lane, y_policy);
           slot ^= 1u;
           if constexpr (kDebug) {
   #pragma unroll 1
@@ -896,6 +1029,11 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.zi = a.zi;
   p.cbsum = a.cbsum;
   p.cbout = a.cbout;
+  p.wout = static_cast<const uint16_t*>(a.wout);
+  p.ncap = a.ncap;
+  p.xoT = static_cast<const uint16_t*>(a.xoT);
+  p.xo_stride = xo_stride(a.T);
+  p.cc_max = kCcMaxDefault;
   p.timeout_ns = a.timeout_ns;
   p.debug_skip_loads = a.debug_skip_loads;
   const int tiles = p.m_tiles * p.n_tiles;

@@ -17,6 +17,11 @@ int sm_count();
 constexpr int kKBlock = 64;         // K elements per pipeline stage (128 bytes of fp16)
 constexpr int kChunkKBlocks = 16;   // K blocks per exact fp32 accumulation chunk (1024 K)
 constexpr int kChunkK = kKBlock * kChunkKBlocks;
+// Outlier columns up to this count are multiplied on the CUDA cores in the tensor-core
+// matmul's epilogue, from a transposed copy of X_out (kCcOutlierCols rows of tokens).
+constexpr int kCcOutlierCols = 32;
+// Token stride of that copy: T rounded up to 16 (16-token slices, 32-byte aligned rows).
+__host__ __device__ inline int xo_stride(int T) { return (T + 15) / 16 * 16; }
 
 // Token tile (MMA N) of the int8 tensor-core matmul for T tokens: the smallest supported
 // size that covers T, 256 for large T. The quantize pass uses it to group its per-chunk
@@ -64,6 +69,7 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 // int8_matmul_workspace_size() and int8_matmul().
 struct WsLayout {
   size_t header = 0, mask = 0, l1 = 0, idx = 0, xq = 0, rowabs = 0, xout = 0, wout = 0;
+  size_t xoT = 0;         // X_out transposed [kCcOutlierCols][xo_stride(T)] fp16
   size_t zi = 0;          // zeropoint variant: int32 per-row zero points [T]
   size_t cbout = 0;       // zeropoint variant: int32 sums of the outlier columns' codes [out]
   size_t acc = 0;         // int32 running sums of the matmul's epilogue, one tile per SM
@@ -102,6 +108,7 @@ inline WsLayout ws_layout(int T, int in, int out, int ncap, bool split_ok = true
   L.rowabs = off; off = align_up(off + 4 * (size_t)T, 256);
   L.xout = off; off = align_up(off + 2 * (size_t)T * ncap, 256);
   L.wout = off; off = align_up(off + 2 * (size_t)out * ncap, 256);
+  L.xoT = off; off = align_up(off + 2 * (size_t)kCcOutlierCols * xo_stride(T), 256);
   L.zi = off; off = align_up(off + 4 * (size_t)T, 256);
   L.cbout = off; off = align_up(off + 4 * (size_t)out, 256);
   L.acc = off; off = align_up(off + 4 * (size_t)sm_count() * 128 * i8_bn(T), 256);
@@ -140,11 +147,12 @@ struct NextLayer {
   uint32_t* mask = nullptr;      // null: no statistics
   uint32_t thr_bits = 0x7C00u;
 };
+// xoT (nullable): X_out transposed, rows k < kCcOutlierCols (zeros past the outlier count).
 cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* CB,
                                    const float* SCB, int out, const WsHeader* hdr,
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
-                                   int32_t* l1, int8_t* xq8_debug, cudaStream_t s);
+                                   void* xoT, int32_t* l1, int8_t* xq8_debug, cudaStream_t s);
 // Zeropoint variant of quantize + gather: per row S, Z over the inlier columns, codes
 // clamp(rint(x*S - Z)) (outlier columns 0) as fp16, the epilogue's row factor
 // rowabs[i] = 127/S (127*min for a constant row) and zero point zi[i] = Z (1 for a constant
@@ -154,13 +162,16 @@ cudaError_t launch_quantize_gather_zp(const void* X, int T, int in, const int8_t
                                       const float* SCB, int out, const WsHeader* hdr,
                                       const uint32_t* mask, const int32_t* idx, int ncap,
                                       void* xq16, float* rowabs, int32_t* zi, void* xout,
-                                      void* wout, int32_t* cbout, int32_t* l1,
+                                      void* wout, void* xoT, int32_t* cbout, int32_t* l1,
                                       int8_t* xq8_debug, float* dbg_S, float* dbg_Z,
                                       cudaStream_t s);
 // Sum of each row's int8 codes: CBsum[o] = sum_j CB[o, j] (int32).
 cudaError_t launch_code_sums(const int8_t* CB, int out, int in, int32_t* CBsum, cudaStream_t s);
 cudaError_t launch_absmax_rows(const void* X, int rows, int cols, int8_t* Q, float* absmax,
                                cudaStream_t s);
+// Block-wise absmax: blocks of `block` columns per row, absmax [rows, ceil(cols / block)].
+cudaError_t launch_absmax_blocks(const void* X, int rows, int cols, int block, int8_t* Q,
+                                 float* absmax, cudaStream_t s);
 cudaError_t launch_zeropoint_rows(const void* X, int rows, int cols, int8_t* Q, float* S,
                                   float* Z, cudaStream_t s);
 
@@ -175,6 +186,9 @@ struct GemmArgs {
   const void* wout = nullptr;
   const void* xout = nullptr;
   int ncap = 0;
+  // X_out transposed [kCcOutlierCols][xo_stride(T)] for the CUDA-core outlier product (null:
+  // the outlier product always runs on the tensor cores)
+  const void* xoT = nullptr;
   WsHeader* hdr = nullptr;      // status word + n_out (int8 path), may be null for fp16
   const float* rowabs = nullptr;
   const int32_t* l1 = nullptr;  // per (token tile, chunk) code-magnitude bounds, or null

@@ -205,6 +205,17 @@ __global__ void __launch_bounds__(kRowThreads) absmax_rows_kernel(
   if (threadIdx.x == 0) amax[row] = a;
 }
 
+// Row i's outlier values into the transposed slice of the matmul's CUDA-core outlier
+// product: xoT[k * xo_stride(T) + i] = X[i, idx[k]] for k < n, 0 for n <= k < kCcOutlierCols.
+__device__ __forceinline__ void gather_transposed(const uint16_t* __restrict__ x,
+                                                  const int32_t* __restrict__ idx, int n,
+                                                  uint16_t* __restrict__ xoT, int T, size_t i) {
+  if (!xoT) return;
+  const size_t stride = xo_stride(T);
+  for (int k = threadIdx.x; k < kCcOutlierCols; k += kRowThreads)
+    xoT[(size_t)k * stride + i] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
+}
+
 // Blocks [T, ..) of the quantize passes: 32 output features per block, 8 threads per
 // feature o: W_out[o, k] = fp16((CB[o,idx[k]]*SCB[o])/127) for k < n, zeros up to npad.
 // Returns, in the feature's first thread, sum_k CB[o, idx[k]] (the other threads: partial).
@@ -243,7 +254,8 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
     const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
     const uint32_t* __restrict__ mask, const int32_t* __restrict__ idx, int ncap,
     uint16_t* __restrict__ xq16, float* __restrict__ rowabs, uint16_t* __restrict__ xout,
-    uint16_t* __restrict__ wout, int32_t* __restrict__ l1, int bn, int8_t* __restrict__ xq8) {
+    uint16_t* __restrict__ wout, uint16_t* __restrict__ xoT, int32_t* __restrict__ l1, int bn,
+    int8_t* __restrict__ xq8) {
   extern __shared__ uint32_t s_mask[];  // (in + 31) / 32 words
   __shared__ uint32_t s_red[kRowThreads / 32];
   __shared__ int s_l1[I8_MAX_IN / kChunkK];
@@ -266,6 +278,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_kernel(
       if (s_l1[c] > 0) atomicMax(&l1[(size_t)(i / bn) * nch + c], s_l1[c]);
     for (int k = threadIdx.x; k < npad; k += kRowThreads)
       xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
+    gather_transposed(x, idx, n, xoT, T, i);
   } else {
     if (npad == 0) return;
     gather_outlier_weights(CB, SCB, in, out, idx, n, npad, ncap, T, wout);
@@ -499,9 +512,9 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_zp_kernel(
     const float* __restrict__ SCB, int out, const WsHeader* __restrict__ hdr,
     const uint32_t* __restrict__ mask, const int32_t* __restrict__ idx, int ncap,
     uint16_t* __restrict__ xq16, float* __restrict__ rowabs, int32_t* __restrict__ zi,
-    uint16_t* __restrict__ xout, uint16_t* __restrict__ wout, int32_t* __restrict__ cbout,
-    int32_t* __restrict__ l1, int bn, int8_t* __restrict__ xq8, float* __restrict__ dbg_S,
-    float* __restrict__ dbg_Z) {
+    uint16_t* __restrict__ xout, uint16_t* __restrict__ wout, uint16_t* __restrict__ xoT,
+    int32_t* __restrict__ cbout, int32_t* __restrict__ l1, int bn, int8_t* __restrict__ xq8,
+    float* __restrict__ dbg_S, float* __restrict__ dbg_Z) {
   extern __shared__ uint32_t s_mask[];  // (in + 31) / 32 words
   __shared__ float s_mn[kRowThreads / 32], s_mx[kRowThreads / 32];
   __shared__ int s_l1[I8_MAX_IN / kChunkK];
@@ -531,6 +544,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_gather_zp_kernel(
       if (s_l1[c] > 0) atomicMax(&l1[(size_t)(i / bn) * nch + c], s_l1[c]);
     for (int k = threadIdx.x; k < npad; k += kRowThreads)
       xout[i * ncap + k] = k < n ? x[__ldg(&idx[k])] : (uint16_t)0;
+    gather_transposed(x, idx, n, xoT, T, i);
   } else {
     const int csum = gather_outlier_weights(CB, SCB, in, out, idx, n, npad, ncap, T, wout);
     const int o = (blockIdx.x - T) * 32 + (threadIdx.x >> 3);
@@ -594,7 +608,7 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
                                    const float* SCB, int out, const WsHeader* hdr,
                                    const uint32_t* mask, const int32_t* idx, int ncap,
                                    void* xq16, float* rowabs, void* xout, void* wout,
-                                   int32_t* l1, int8_t* xq8_debug, cudaStream_t s) {
+                                   void* xoT, int32_t* l1, int8_t* xq8_debug, cudaStream_t s) {
   // without a W_out buffer (the decode path reads the outlier weights from CB itself) only
   // the T row blocks run
   const int wblocks = wout ? (out + 31) / 32 : 0;
@@ -603,7 +617,7 @@ cudaError_t launch_quantize_gather(const void* X, int T, int in, const int8_t* C
   quantize_gather_kernel<NV><<<T + wblocks, kRowThreads, smem, s>>>(                         \
       static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,           \
       static_cast<uint16_t*>(xq16), rowabs, static_cast<uint16_t*>(xout),                   \
-      static_cast<uint16_t*>(wout), l1, i8_bn(T), xq8_debug)
+      static_cast<uint16_t*>(wout), static_cast<uint16_t*>(xoT), l1, i8_bn(T), xq8_debug)
   I8_DISPATCH_NV(in, I8_LAUNCH)
 #undef I8_LAUNCH
   return cudaGetLastError();
@@ -613,7 +627,7 @@ cudaError_t launch_quantize_gather_zp(const void* X, int T, int in, const int8_t
                                       const float* SCB, int out, const WsHeader* hdr,
                                       const uint32_t* mask, const int32_t* idx, int ncap,
                                       void* xq16, float* rowabs, int32_t* zi, void* xout,
-                                      void* wout, int32_t* cbout, int32_t* l1,
+                                      void* wout, void* xoT, int32_t* cbout, int32_t* l1,
                                       int8_t* xq8_debug, float* dbg_S, float* dbg_Z,
                                       cudaStream_t s) {
   const int wblocks = (out + 31) / 32;
@@ -622,7 +636,8 @@ cudaError_t launch_quantize_gather_zp(const void* X, int T, int in, const int8_t
   quantize_gather_zp_kernel<NV><<<T + wblocks, kRowThreads, smem, s>>>(                      \
       static_cast<const uint16_t*>(X), T, in, CB, SCB, out, hdr, mask, idx, ncap,           \
       static_cast<uint16_t*>(xq16), rowabs, zi, static_cast<uint16_t*>(xout),               \
-      static_cast<uint16_t*>(wout), cbout, l1, i8_bn(T), xq8_debug, dbg_S, dbg_Z)
+      static_cast<uint16_t*>(wout), static_cast<uint16_t*>(xoT), cbout, l1, i8_bn(T),        \
+      xq8_debug, dbg_S, dbg_Z)
   I8_DISPATCH_NV(in, I8_LAUNCH)
 #undef I8_LAUNCH
   return cudaGetLastError();

@@ -109,6 +109,11 @@ def test_other_entry_points_validate(L):
     assert L.int8_quantize_weight(fake(A), 0, 16, fake(A), fake(A), None) == 0
     assert L.absmax_quantize_rows(fake(A), -1, 8, fake(A), fake(A), None) == 1
     assert L.absmax_quantize_rows(fake(A), 0, 8, fake(A), fake(A), None) == 0
+    assert L.absmax_quantize_blocks(fake(A), 2, 8, 0, fake(A), fake(A), None) == 1
+    assert L.absmax_quantize_blocks(fake(A), 2, 8, 64, fake(A), None, None) == 1
+    assert L.absmax_quantize_blocks(fake(A), 2, 8, 64, fake(A + 2), fake(A), None) == 2
+    assert L.absmax_quantize_blocks(fake(A), 0, 8, 64, fake(A), fake(A), None) == 0
+    assert L.absmax_quantize_blocks(fake(A), 3, 0, 64, fake(A), fake(A), None) == 0
     assert L.zeropoint_quantize_rows(fake(A), 2, 8, None, fake(A), fake(A), None) == 1
     assert L.zeropoint_quantize_rows(fake(A), 2, 8, fake(A), fake(A + 4), fake(A), None) == 2
     assert L.f16_matmul(fake(A), 4, 20, fake(A), 8, None, fake(A), None) == 2

@@ -249,6 +249,24 @@ def test_absmax_rows_bit_exact(i8, rows, cols):
     np.testing.assert_array_equal(a.cpu().numpy(), ao)
 
 
+@pytest.mark.parametrize("rows,cols,block", [
+    (1024, 8192, 64), (1024, 8192, 128),      # the sweep's X, the pages' block sizes
+    (37, 1000, 64),                            # ragged last block (1000 = 15 * 64 + 40)
+    (5, 200, 16), (3, 4104, 256), (9, 520, 32),
+    (7, 100, 64),                              # cols % 8 != 0 (element path)
+    (4, 96, 48), (2, 5, 3), (3, 64, 1000),     # other block sizes, one block per row
+])
+def test_absmax_blocks_bit_exact(i8, rows, cols, block):
+    X = synth.make_random_f16(rows * 7 + cols + block, (rows, cols), std=1.5)
+    g = np.random.default_rng(block)
+    X *= np.exp2(g.integers(-4, 5, (rows, 1))).astype(np.float16)  # rows of different scales
+    X[0, : min(cols, block)] = 0                                     # a zero block
+    Q, a = i8.absmax_quantize_blocks(dev(X), block)
+    Qo, ao = oracle.quantize_blocks_absmax(X, block)
+    np.testing.assert_array_equal(Q.cpu().numpy(), Qo)
+    np.testing.assert_array_equal(a.cpu().numpy(), ao)
+
+
 @pytest.mark.parametrize("rows,cols", [(1024, 8192), (4, 9), (6, 1000), (3, 1)])
 def test_zeropoint_rows_bit_exact(i8, rows, cols):
     w = synth.Workload("zp", rows, cols, 1)
