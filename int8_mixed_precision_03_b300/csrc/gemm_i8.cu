@@ -56,6 +56,17 @@
 // reaches TMEM lanes 32*(w%4) .. +31). Persistent CTAs, one per SM, walk tiles
 // token-block fastest so that concurrently running CTAs share the same weight strip in L2.
 //
+// CTA pairs: 256-token tiles on the whole-tile schedule run on clusters of two CTAs (two
+// SMs) that share one tile of 256 output features x 256 tokens through tcgen05 cta_group::2
+// MMAs with M = 256: CTA r (its rank in the pair) converts and holds A rows 128r .. 128r + 127
+// and holds B rows (tokens) 128r .. 128r + 127, and its TMEM receives its 128 feature rows of
+// the accumulator for all 256 tokens. The even CTA issues the MMAs; both CTAs' B halves
+// complete on its barrier (TMA with .cta_group::2), the odd CTA's converter and epilogue
+// warps arrive on its barriers remotely, and its commits reach both CTAs (multicast). Per
+// SM the tensor core reads half of B per K block instead of all of it, which halves the
+// operand traffic of the shared-memory port and lets B stages be half as large. The
+// epilogue is unchanged: each CTA writes its own 128 features.
+//
 // Schedules: whole tiles per CTA (t = b, b + G, ...), or, where that leaves the last wave
 // unbalanced (i8_split_ctas), the split schedule (kSplit): the (tile, 1024-K chunk) units
 // are cut into one contiguous range per CTA, and a tile cut into pieces is finished by the
@@ -78,16 +89,21 @@ static_assert(kCcOut == 32, "one transposed X_out row per lane");
 // Largest outlier count sent to the CUDA-core path (<= kCcOut): above it the outlier
 // product is cheaper as an MMA segment than as per-element work in the epilogue.
 constexpr int kCcMaxDefault = 32;
+// 256-token tiles run on CTA pairs (cta_group::2) unless this is set.
+constexpr bool kDisablePairs = false;
 constexpr uint32_t kWorstChunkBound = 127u * 127u * kChunkK;  // < kExactLimit
 static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact");
 
-template <int BN>
+template <int BN, bool kPair = false>
 struct Cfg {
   static constexpr int kW = 16;  // tokens per epilogue slice
-  // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring
-  static constexpr int kStages = BN == 256 ? 3 : 4;
+  // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring. A CTA of
+  // a pair holds half of the tile's B rows, so its stages are half as large and it affords
+  // one more of them.
+  static constexpr int kStages = kPair ? 4 : BN == 256 ? 3 : 4;
   static constexpr int kStages8 = BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBRows = kPair ? BN / 2 : BN;  // B rows (tokens) in this CTA's stages
+  static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kBoxBytes = kW * 32 * 2;
   static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN;  // F0 + F1
   // shared memory (stage bases 1024-byte aligned for the swizzled layouts)
@@ -147,7 +163,14 @@ struct Params {
 // The pieces of work of one CTA: whole tiles t = b, b + G, ... (unsplit), or the runs of
 // its unit range that fall in one tile (split). A piece is (tile t, chunks [c0, c1)); its K
 // blocks are [16 c0, min(16 c1, nkb)) plus the outlier K blocks when c1 == nchunks.
-template <bool kSplit>
+// First tile and tile stride of this CTA's whole-tile schedule: CTA b of a single-CTA grid,
+// or the pair (cluster) b / 2 of a grid of CTA pairs, whose two CTAs work on the same tiles.
+template <bool kPair>
+__device__ __forceinline__ int tile_first() { return kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x; }
+template <bool kPair>
+__device__ __forceinline__ int tile_stride() { return kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
+
+template <bool kSplit, bool kPair = false>
 struct Sched {
   long long u = 0, ue = 0;
   int t = 0;
@@ -156,7 +179,7 @@ struct Sched {
       u = p.units * blockIdx.x / gridDim.x;
       ue = p.units * (blockIdx.x + 1) / gridDim.x;
     } else {
-      t = blockIdx.x;
+      t = tile_first<kPair>();
     }
   }
   __device__ bool next(const Params& p, int& tt, int& c0, int& c1) {
@@ -165,7 +188,7 @@ struct Sched {
       tt = t;
       c0 = 0;
       c1 = p.nchunks;
-      t += gridDim.x;
+      t += tile_stride<kPair>();
       return true;
     }
     if (u >= ue) return false;
@@ -306,13 +329,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int BN, int kMode, bool kSplit>
+// Pipeline waits (the same in a CTA pair: see mbar_arrive_cluster for the arrivals).
+template <bool kPair>
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, const Abort& ab) {
+  return pipe_wait(bar, parity, ab);
+}
+template <bool kPair>
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t ns) {
+  return mbar_wait_bounded(bar, parity, ns);
+}
+// Arrival on a barrier of the pair's even CTA (the MMA issuer's), or a local arrival.
+template <bool kPair>
+__device__ __forceinline__ void arrive_leader(uint64_t* bar) {
+  if constexpr (kPair) {
+    if (cluster_ctarank() == 0) mbar_arrive(bar);
+    else mbar_arrive_cluster(mapa_rank(bar, 0));
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+template <int BN, int kMode, bool kSplit, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmWo, const __grid_constant__ CUtensorMap tmXo,
                    const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using C = Cfg<BN>;
+  static_assert(!kPair || (BN == 256 && !kSplit), "CTA pairs run 256-token whole tiles");
+  using C = Cfg<BN, kPair>;
   constexpr int kS = C::kStages, kS8 = C::kStages8, kW = C::kW;
+  // rank in the CTA pair (0 = the MMA issuer) and this CTA's share of a tile: feature rows
+  // [128 rank, 128 rank + 128) of the 256 (pair) or 128 rows, B rows (tokens) likewise
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  constexpr int kFeatTile = kPair ? 2 * BM : BM;
   constexpr bool kDebug = kMode == kEpiDebug || kMode == kEpiZpDebug;
   constexpr bool kNext = kMode == kEpiNext;
   constexpr bool kZp = kMode == kEpiZp || kMode == kEpiZpDebug;
@@ -333,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kS; ++s) {
-      mbar_init(&full_a[s], 4);      // the four warps of the converter set
+      mbar_init(&full_a[s], kPair ? 8 : 4);  // the four warps of the converter set (each CTA's)
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -343,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tmem_full[s], 1);
-      mbar_init(&tmem_empty[s], 4);  // one arrival per epilogue warp
+      mbar_init(&tmem_empty[s], kPair ? 8 : 4);  // one arrival per epilogue warp (each CTA's)
     }
     mbar_init(done, 1);
     mbar_init(epi_bar, 4);
@@ -360,11 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmWo);
   }
   if (warp == kWarpMma) {
-    tmem_alloc(tmem_base_smem, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_base_smem, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_base_smem, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_smem;
 
@@ -385,25 +439,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t keep = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      Sched<kSplit> sc(p);
+      Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
-        const int n0 = (t % p.n_tiles) * BN;
+        const int n0 = (t % p.n_tiles) * BN + (int)rank * C::kBRows;  // this CTA's B rows
         const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
         for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb, ++it) {
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
-          if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
-          mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
-          if (kb < p.nkb)
-            tma_load_2d_hint(smem + C::b + s * C::kBBytes, &tmB, &full_b[s], kb * BK, n0, keep);
-          else
-            tma_load_2d(smem + C::b + s * C::kBBytes, &tmXo, &full_b[s], (kb - p.nkb) * BK, n0);
+          if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
+          uint8_t* dst = smem + C::b + s * C::kBBytes;
+          if constexpr (kPair) {
+            // both halves complete on the MMA issuer's barrier, which expects both
+            if (rank == 0) mbar_arrive_expect_tx(&full_b[s], 2 * C::kBBytes);
+            const uint32_t bar = mapa_rank(&full_b[s], 0);
+            if (kb < p.nkb)
+              tma_load_2d_pair(dst, &tmB, bar, kb * BK, n0, keep);
+            else
+              tma_load_2d_pair(dst, &tmXo, bar, (kb - p.nkb) * BK, n0, keep);
+          } else {
+            mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
+            if (kb < p.nkb)
+              tma_load_2d_hint(dst, &tmB, &full_b[s], kb * BK, n0, keep);
+            else
+              tma_load_2d(dst, &tmXo, &full_b[s], (kb - p.nkb) * BK, n0);
+          }
         }
       }
-      // Do not leave the CTA with copies in flight: wait for the last issued stages.
-      for (uint32_t k = 0; k < (uint32_t)kS && k < it; ++k) {
-        const uint32_t j = it - 1 - k;
-        mbar_wait_bounded(&full_b[j % kS], (j / kS) & 1u, p.timeout_ns);
+      // Do not leave the CTA with copies in flight: wait for the last issued stages (in a
+      // pair the issuer's barrier counts both CTAs' copies, and the peer leaves only after
+      // the issuer, at the final cluster barrier).
+      if (rank == 0) {
+        for (uint32_t k = 0; k < (uint32_t)kS && k < it; ++k) {
+          const uint32_t j = it - 1 - k;
+          wait_bounded<kPair>(&full_b[j % kS], (j / kS) & 1u, p.timeout_ns);
+        }
       }
     }
   } else if (warp == kWarpA8) {
@@ -412,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !p.debug_skip_loads) {
       uint32_t i8 = 0;
       bool ok = true;
-      Sched<kSplit> sc(p);
+      Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
-        const int m0 = (t / p.n_tiles) * BM;
+        const int m0 = (t / p.n_tiles) * kFeatTile + (int)rank * BM;
         const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
         for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb) {
           const int nbox = kb < p.nkb ? 1 : 2;
@@ -438,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32acc(BM, BN);
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_f16_f32acc(kPair ? 2 * BM : BM, BN);
       uint32_t it = 0, nseg = 0;
       bool ok = true;
-      Sched<kSplit> sc(p);
+      Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
         const int n_blk = t % p.n_tiles;
@@ -465,32 +534,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             opens = kb == p.nkb;
           }
           if (opens) {
-            if (kb > kb_lo) { mma_commit(&tmem_full[nseg & 1u]); ++nseg; }
-            if (!(ok = pipe_wait(&tmem_empty[nseg & 1u], ((nseg >> 1) & 1u) ^ 1u, ab))) break;
+            if (kb > kb_lo) {
+              if constexpr (kPair) mma_commit_pair(&tmem_full[nseg & 1u], 3);
+              else mma_commit(&tmem_full[nseg & 1u]);
+              ++nseg;
+            }
+            if (!(ok = pwait<kPair>(&tmem_empty[nseg & 1u], ((nseg >> 1) & 1u) ^ 1u, ab))) break;
             tc_fence_after();
             dcol = (nseg & 1u) * BN;
             seg_first = true;
           }
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
-          if (!(ok = pipe_wait(&full_a[s], ph, ab))) break;
-          if (!(ok = pipe_wait(&full_b[s], ph, ab))) break;
+          if (!(ok = pwait<kPair>(&full_a[s], ph, ab))) break;
+          if (!(ok = pwait<kPair>(&full_b[s], ph, ab))) break;
           tc_fence_after();
           const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
           const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBBytes);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
-                       (seg_first && k == 0) ? 0u : 1u);
+          for (int k = 0; k < BK / 16; ++k) {
+            if constexpr (kPair)
+              mma_f16_ss_pair(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
+                              (seg_first && k == 0) ? 0u : 1u);
+            else
+              mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
+                         (seg_first && k == 0) ? 0u : 1u);
+          }
           seg_first = false;
-          mma_commit(&empty[s]);
+          if constexpr (kPair) mma_commit_pair(&empty[s], 3);
+          else mma_commit(&empty[s]);
         }
         if (!ok) break;
-        mma_commit(&tmem_full[nseg & 1u]);
+        if constexpr (kPair) mma_commit_pair(&tmem_full[nseg & 1u], 3);
+        else mma_commit(&tmem_full[nseg & 1u]);
         ++nseg;
       }
-      // all issued MMAs have completed before TMEM is released
-      mma_commit(done);
-      mbar_wait_bounded(done, 0, p.timeout_ns);
+      // all issued MMAs have completed before TMEM is released (in both CTAs of a pair)
+      if constexpr (kPair) mma_commit_pair(done, 3);
+      else mma_commit(done);
+      wait_bounded<kPair>(done, 0, p.timeout_ns);
+    } else if (kPair && lane == 0) {
+      wait_bounded<kPair>(done, 0, p.timeout_ns);  // the issuer's MMAs, before TMEM is freed
     }
   } else if ((warp >= kWarpConv0 && warp < kWarpConv0 + 4) || warp >= kWarpConv1) {
     // -------------------------------------------------------- weights into fp16 A
@@ -506,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t swz16 = (uint32_t)r & 7u;
       uint32_t it = 0, i8 = 0;
       bool ok = true;
-      Sched<kSplit> sc(p);
+      Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
         const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
@@ -517,11 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((int)(it & 1u) != set) continue;  // K block `it` belongs to set it & 1
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
           // the MMAs that last read A stage s have completed
-          if (!(ok = pipe_wait(&empty[s], ph ^ 1u, ab))) break;
+          if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
           uint32_t a[32];
           if (is_int) {
             const uint32_t s8 = i8_0 % kS8;
-            if (!(ok = pipe_wait(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
+            if (!(ok = pwait<kPair>(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
             const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
             uint4 v[4];
 #pragma unroll
@@ -537,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
-              if (!(ok = pipe_wait(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
+              if (!(ok = pwait<kPair>(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
               const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
@@ -562,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             mbar_arrive(&a8_empty[i8_0 % kS8]);
             if (!is_int) mbar_arrive(&a8_empty[(i8_0 + 1) % kS8]);
-            mbar_arrive(&full_a[s]);
+            arrive_leader<kPair>(&full_a[s]);
           }
         }
       }
@@ -581,9 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
       uint32_t nseg = 0, slot = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = tile_first<kPair>(); t < tiles && ok; t += tile_stride<kPair>()) {
         const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
-        const int m0 = m_blk * BM, n0 = n_blk * BN;
+        const int m0 = m_blk * kFeatTile + (int)rank * BM, n0 = n_blk * BN;
         const int o = m0 + q * 32 + lane;
         const bool o_ok = o < p.out;
         const float bo = (o_ok && p.bias) ? __half2float(__ushort_as_half(p.bias[o])) : 0.0f;
@@ -609,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool first = si == 0;
           const bool last = si == nseg_tile - 1;
           const uint32_t b = nseg & 1u;
-          if (!(ok = pipe_wait(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
+          if (!(ok = pwait<kPair>(&tmem_full[b], (nseg >> 1) & 1u, ab))) break;
           tc_fence_after();
           const uint32_t tF = tq + b * BN;
           // Running sums of the tile (not for its first segment): slice j0's are in pc while
@@ -642,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the accumulator is free as soon as it has been read
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tmem_empty[b]);
+            if (lane == 0) arrive_leader<kPair>(&tmem_empty[b]);
           } else {
   #pragma unroll 1
             for (int j0 = 0; j0 < BN; j0 += kW) {
@@ -665,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j0 + kW >= BN) {  // all of F has been read: release it to the MMA
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tmem_empty[b]);
+                if (lane == 0) arrive_leader<kPair>(&tmem_empty[b]);
               }
               const float ra_s = ra[0];  // this slice's tokens, one per lane
               [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
@@ -957,43 +1040,128 @@ __global__ void __launch_bounds__(kThreads, 1)
   // -------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  // a pair's CTAs leave together: neither exits while the other may still arrive on its
+  // barriers or read its shared memory through the MMAs
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == kWarpMma) {
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
+  }
 }
 
-template <int BN, int kMode, bool kSplit>
-cudaError_t launch_split(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
-                         const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
-                         const Params& p, int grid) {
-  using C = Cfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(i8_gemm_kernel<BN, kMode, kSplit>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
+template <int BN, int kMode, bool kSplit, bool kPair>
+cudaError_t launch_variant(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
+                           const CUtensorMap& mWo, const CUtensorMap& mXo,
+                           const CUtensorMap& mY, const Params& p, int grid) {
+  using C = Cfg<BN, kPair>;
+  auto kernel = i8_gemm_kernel<BN, kMode, kSplit, kPair>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::total);
   if (e != cudaSuccess) return e;
-  i8_gemm_kernel<BN, kMode, kSplit><<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
-  return cudaGetLastError();
+  if constexpr (!kPair) {
+    kernel<<<grid, kThreads, C::total, s>>>(mA8, mB, mWo, mXo, mY, p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, mA8, mB, mWo, mXo, mY, p);
+  }
+}
+
+// Pairs of CTAs (2-SM clusters) that can be resident at once for this kernel, looked up once
+// per device; 0 if the device cannot run it.
+template <int kMode>
+int max_pairs() {
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {};  // 0: not looked up yet, -1: none
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cache[dev] == 0) {
+    using C = Cfg<256, true>;
+    auto kernel = i8_gemm_kernel<256, kMode, false, true>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::total) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * sm_count(), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = C::total;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache[dev] = n > 0 ? n : -1;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
 }
 
 template <int BN, int kMode>
 cudaError_t launch_kernel(cudaStream_t s, const CUtensorMap& mA8, const CUtensorMap& mB,
                           const CUtensorMap& mWo, const CUtensorMap& mXo, const CUtensorMap& mY,
-                          const Params& p, int grid) {
-  if (p.split) return launch_split<BN, kMode, true>(s, mA8, mB, mWo, mXo, mY, p, grid);
-  return launch_split<BN, kMode, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
+                          const Params& p, int grid, bool pair) {
+  if constexpr (BN == 256) {
+    if (pair) return launch_variant<BN, kMode, false, true>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  }
+  if (p.split) return launch_variant<BN, kMode, true, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  return launch_variant<BN, kMode, false, false>(s, mA8, mB, mWo, mXo, mY, p, grid);
+}
+
+// Kernel mode of a call (the epilogue variant).
+inline int epi_mode(const GemmArgs& a) {
+  if (a.zi) return a.acc_debug ? kEpiZpDebug : kEpiZp;
+  if (a.next.mask) return kEpiNext;
+  return a.acc_debug ? kEpiDebug : kEpiPlain;
 }
 
 template <int BN>
 cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
+  // 256-token tiles on the whole-tile schedule run on CTA pairs (M = 256 per MMA, each CTA
+  // holding half of the tile's B rows) when the device can hold at least one pair
+  int pairs = 0;
+  if constexpr (BN == 256) {
+    if (!a.split && !kDisablePairs) {
+      switch (epi_mode(a)) {
+        case kEpiPlain: pairs = max_pairs<kEpiPlain>(); break;
+        case kEpiDebug: pairs = max_pairs<kEpiDebug>(); break;
+        case kEpiNext: pairs = max_pairs<kEpiNext>(); break;
+        case kEpiZp: pairs = max_pairs<kEpiZp>(); break;
+        default: pairs = max_pairs<kEpiZpDebug>(); break;
+      }
+    }
+  }
+  const bool pair = pairs > 0;
+  const int b_rows = pair ? BN / 2 : BN;  // B rows per CTA and stage
   using C = Cfg<BN>;
   CUtensorMap mA8, mB, mWo, mXo, mY;
   bool ok = true;
   ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM, BK,
                  CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= make_map(&mB, a.b_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.in, BN, BK,
+  ok &= make_map(&mB, a.b_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.in, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   // outlier weights: 128 rows x 32 fp16 (64 bytes) per box, two boxes per K block
   ok &= make_map(&mWo, a.wout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out, a.ncap, BM, BK / 2,
                  CU_TENSOR_MAP_SWIZZLE_64B);
-  ok &= make_map(&mXo, a.xout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.ncap, BN, BK,
+  ok &= make_map(&mXo, a.xout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.ncap, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   // Y [T, out] fp16 through TMA stores when its row pitch is a multiple of 16 bytes
   const bool y_tma = (a.out % 8) == 0;
@@ -1007,7 +1175,7 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   p.T = a.T;
   p.in = a.in;
   p.out = a.out;
-  p.m_tiles = (a.out + BM - 1) / BM;
+  p.m_tiles = (a.out + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   p.n_tiles = (a.T + BN - 1) / BN;
   p.nkb = (a.in + BK - 1) / BK;
   p.nchunks = num_chunks(a.in);
@@ -1039,6 +1207,7 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   const int tiles = p.m_tiles * p.n_tiles;
   const int sms = sm_count();
   int grid = tiles < sms ? tiles : sms;
+  if (pair) grid = 2 * (tiles < pairs ? tiles : pairs);  // whole clusters, one per tile at most
   p.split = 0;
   if (a.split) {  // cut tiles between CTAs by 1024-K chunks (see i8_split_ctas)
     if (!a.part || !a.part_f || !a.tile_cnt) return cudaErrorInvalidValue;
@@ -1053,13 +1222,14 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   if ((a.next.relu && !a.next.mask) || (a.next.mask && (a.acc_debug || a.zi)))
     return cudaErrorInvalidValue;
   if (a.zi && (!a.cbsum || !a.cbout)) return cudaErrorInvalidValue;
-  if (a.zi) {
-    if (a.acc_debug) return launch_kernel<BN, kEpiZpDebug>(s, mA8, mB, mWo, mXo, mY, p, grid);
-    return launch_kernel<BN, kEpiZp>(s, mA8, mB, mWo, mXo, mY, p, grid);
+  switch (epi_mode(a)) {
+    case kEpiZpDebug:
+      return launch_kernel<BN, kEpiZpDebug>(s, mA8, mB, mWo, mXo, mY, p, grid, pair);
+    case kEpiZp: return launch_kernel<BN, kEpiZp>(s, mA8, mB, mWo, mXo, mY, p, grid, pair);
+    case kEpiNext: return launch_kernel<BN, kEpiNext>(s, mA8, mB, mWo, mXo, mY, p, grid, pair);
+    case kEpiDebug: return launch_kernel<BN, kEpiDebug>(s, mA8, mB, mWo, mXo, mY, p, grid, pair);
+    default: return launch_kernel<BN, kEpiPlain>(s, mA8, mB, mWo, mXo, mY, p, grid, pair);
   }
-  if (a.next.mask) return launch_kernel<BN, kEpiNext>(s, mA8, mB, mWo, mXo, mY, p, grid);
-  if (a.acc_debug) return launch_kernel<BN, kEpiDebug>(s, mA8, mB, mWo, mXo, mY, p, grid);
-  return launch_kernel<BN, kEpiPlain>(s, mA8, mB, mWo, mXo, mY, p, grid);
 }
 
 }  // namespace

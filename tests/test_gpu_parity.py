@@ -321,10 +321,13 @@ def test_full_size_config_sampled_rows(i8, name):
         assert set(planted.tolist()) <= set(ref["idx"].tolist())
 
 
-def test_stalled_matmul_times_out_and_the_context_stays_usable(i8):
+@pytest.mark.parametrize("T", [64, 300])
+def test_stalled_matmul_times_out_and_the_context_stays_usable(i8, T):
     """Every pipeline wait of the tensor-core matmul runs out (its loaders load nothing):
-    the kernel records I8_ERR_TIMEOUT and returns; the next call on the stream is correct."""
-    w = synth.Workload("stall", 64, 256, 256, n_outlier_cols=2, seed=5)
+    the kernel records I8_ERR_TIMEOUT and returns; the next call on the stream is correct.
+    64 tokens run on single CTAs, 300 (256-token tiles) on CTA pairs, whose two CTAs both
+    unwind and leave together."""
+    w = synth.Workload("stall", T, 256, 256, n_outlier_cols=2, seed=5)
     X, W, bias = synth.make_x(w), synth.make_w(w), synth.make_bias(w)
     Xd = dev(X)
     CB, SCB = i8.int8_quantize_weight(dev(W))
