@@ -160,6 +160,44 @@ def roofline(w: synth.Workload, matmul_ms: float, peaks: dict, peak_src: str,
                            "product runs on kind::f16, at the bf16/fp16 rate"}
 
 
+# ------------------------------------------------------------------ timing helpers
+L2_NOTE = ("flushed between timed steps: 256 MiB written, then another 256 MiB read, so that "
+           "each timed step starts from a cold L2 holding no dirty lines (untimed)")
+
+
+class L2Flush:
+    """L2 flush between timed steps. Writing a buffer larger than L2 evicts everything, but
+    leaves L2 full of dirty lines whose write-back would then compete with the timed kernels
+    for DRAM; reading a second buffer of the same size afterwards writes them back before
+    the timed step starts."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self, k: int) -> None:
+        import torch
+        self.w.fill_(k & 0xff)
+        torch.amax(self.r)
+
+
+def event_time_us(fn, flush, n: int = 20, warm: int = 3) -> float:
+    """Mean CUDA-event time of fn() in microseconds, L2 flushed before each call."""
+    import torch
+    out = []
+    for k in range(n + warm):
+        flush(k)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        if k >= warm:
+            out.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in out) * 1e3
+
+
 # ------------------------------------------------------------------ distributed plumbing
 def dist_env() -> tuple[int, int, int]:
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -373,7 +411,7 @@ def run_ours(args) -> None:
     CB, SCB = i8.int8_quantize_weight(Wd)        # once per weight, off the timed path
     ws = i8.alloc_workspace(w.T, w.d_in, w.d_out, device)
     Y = torch.empty((w.T, w.d_out), dtype=torch.float16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     zp = args.zeropoint
     if zp:   # zeropoint activation codes; the weight's code sums are prepared with CB
         sums = i8.int8_weight_code_sums(CB)
@@ -409,7 +447,7 @@ def run_ours(args) -> None:
         clocks.mark_start()
     launches = 0
     for k in range(K):
-        flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
+        flush(k)                                  # L2 flush between timed steps (not timed)
         i8.i8_set_profile_events(ev[k])
         step()
         launches += 3                             # our kernels: colstats, quantize, matmul
@@ -472,18 +510,16 @@ def run_ours(args) -> None:
     Ypin = Ype[0]
 
     # our fp16 GEMM on the same shape (the 16-bit comparator), L2 flushed between launches
-    f16_ms = []
-    for k in range(Ke + 3):
-        flush.fill_(k & 0xff)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        i8.f16_matmul(X, Wd, bias, Y=Y)
-        b.record()
-        if k >= 3:
-            f16_ms.append((a, b))
-    torch.cuda.synchronize()
-    f16_ms = statistics.mean(a.elapsed_time(b) for a, b in f16_ms)
+    f16_ms = event_time_us(lambda: i8.f16_matmul(X, Wd, bias, Y=Y), flush, Ke) / 1e3
     del Wd
+    # Streaming references at the same sizes, timed the same way: reading X (the column
+    # statistics read X once) and an fp16 -> fp16 copy of X (the quantize pass reads X and
+    # writes codes of the same size); what any single launch of that traffic takes here.
+    Xc = torch.empty(X.shape, dtype=torch.int8 if uses_gemv(w) else torch.float16,
+                     device=device)
+    ref_us = {"colstats": event_time_us(lambda: torch.amax(X), flush, Ke),
+              "quantize_gather": event_time_us(lambda: Xc.copy_(X), flush, Ke)}
+    del Xc
 
     if rank != 0:
         dist.destroy_process_group()
@@ -499,8 +535,9 @@ def run_ours(args) -> None:
                    "threshold": w.threshold, "n_outlier_cols": w.n_outlier_cols,
                    "activation_codes": "zeropoint" if zp else "absmax",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+                   "l2": L2_NOTE},
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
+        "prepass_gbs": prepass_gbs(w, k_ms, ref_us, peaks),
         "roofline": roof,
         "e2e": {"value": e2e_ops / e2e_s / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(Xpin.numel() * 2),
@@ -542,7 +579,7 @@ def run_ffn(args) -> None:
                      device=device)
     H = torch.empty((f.T, f.d_ff), dtype=torch.float16, device=device)
     Y = torch.empty((f.T, f.d_model), dtype=torch.float16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     thr = f.threshold
 
     def step(x=X, h=H, y=Y, w=ws):
@@ -565,7 +602,7 @@ def run_ffn(args) -> None:
     clocks.mark_start()
     launches = 0
     for k in range(K):
-        flush.fill_(k & 0xff)                     # L2 flush between timed steps (not timed)
+        flush(k)                                  # L2 flush between timed steps (not timed)
         i8.i8_set_profile_events(ev[k])
         st[k].record()
         step()
@@ -588,17 +625,7 @@ def run_ffn(args) -> None:
     value = ops / (step_ms / 1e3) / 1e12
 
     def timed(fn, n):
-        out = []
-        for k in range(n + 3):
-            flush.fill_(k & 0xff)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            if k >= 3:
-                out.append((a, b))
-        torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in out)
+        return event_time_us(fn, flush, n) / 1e3
 
     Kc = min(K, 50)
     ws_u = i8.alloc_workspace(f.T, f.d_model, f.d_ff, device)
@@ -660,7 +687,7 @@ def run_ffn(args) -> None:
                    "threshold": thr, "act": "relu",
                    "n_outlier_cols_x": f.x_workload().n_outlier_cols,
                    "n_outlier_features_h": f.n_h_outliers(), "parallelism": "single",
-                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+                   "l2": L2_NOTE},
         "kernels_us": {k: round(v * 1e3, 2) for k, v in k_ms.items()},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
@@ -686,46 +713,69 @@ def run_ffn(args) -> None:
 
 
 def run_rows(args) -> None:
-    """Standalone row quantizers on the sweep's X [1024, 8192] (absmax on N(0,1) with the
-    sweep's outliers, zeropoint on |N(0,1)|): HBM-bound, reported in GB/s."""
+    """Standalone quantizers, HBM-bound, reported in GB/s: row-wise absmax and zeropoint and
+    block-wise absmax (blocks of 64 and 128) on the sweep's X [1024, 8192] (absmax on N(0,1)
+    with the sweep's outliers, zeropoint on |N(0,1)|), and the same on 16 times as many rows
+    (268 MB of input, twice the L2), where one launch's fixed cost no longer dominates.
+    Beside each, the time of a plain fp16 -> int8 copy of X timed the same way: the same
+    traffic (2 bytes read and 1 written per value) through a library streaming kernel."""
     import torch
     import int8_mixed_precision_03_b300 as i8
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     peaks, peak_src = load_peaks()
-    w = synth.WORKLOADS["sweep_f0.1_thr6"]
-    inputs = {"absmax_quantize_rows": synth.make_x(w), "zeropoint_quantize_rows":
-              synth.make_relu_like(w)}
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    for name, Xh in inputs.items():
-        X = torch.from_numpy(Xh).to(device)
-        fn = getattr(i8, name)
-        for _ in range(max(args.warmup, 3)):
-            fn(X)
-        times = []
-        for k in range(args.steps):
-            flush.fill_(k & 0xff)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn(X)
-            b.record()
-            times.append((a, b))
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in times)
-        rows, cols = Xh.shape
-        nbytes = 2 * rows * cols + rows * cols + (8 if "zero" in name else 4) * rows
-        gbs = nbytes / (ms / 1e3) / 1e9
-        print(json.dumps({
-            "metric": f"{name} GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "dtype": "s8", "data": "synthetic",
-            "config": {"workload": f"{name} [{rows}, {cols}]",
-                       "l2": "flushed between timed steps (256 MiB write, untimed)"},
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
-                         "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
-                         "traffic": None, "algorithmic_bytes": nbytes,
-                         "peak_source": f"hbm_gbs, {peak_src} (MEASURED_PEAKS.json)"}}),
-              flush=True)
+    hbm = float(peaks["hbm_gbs"])
+    flush = L2Flush(device)
+    base = synth.WORKLOADS["sweep_f0.1_thr6"]
+    for rows in (base.T, 16 * base.T):
+        w = base.with_(T=rows)
+        Xa = torch.from_numpy(synth.make_x(w)).to(device)
+        Xz = torch.from_numpy(synth.make_relu_like(w)).to(device)
+        cols = w.d_in
+        Qc = torch.empty((rows, cols), dtype=torch.int8, device=device)
+        ref_us = event_time_us(lambda: Qc.copy_(Xa), flush, args.steps, max(args.warmup, 3))
+        cases = [("absmax_quantize_rows", lambda: i8.absmax_quantize_rows(Xa), 4 * rows),
+                 ("zeropoint_quantize_rows", lambda: i8.zeropoint_quantize_rows(Xz), 8 * rows),
+                 ("absmax_quantize_blocks[64]", lambda: i8.absmax_quantize_blocks(Xa, 64),
+                  4 * rows * cols // 64),
+                 ("absmax_quantize_blocks[128]", lambda: i8.absmax_quantize_blocks(Xa, 128),
+                  4 * rows * cols // 128)]
+        for name, fn, scale_bytes in cases:
+            us = event_time_us(fn, flush, args.steps, max(args.warmup, 3))
+            nbytes = 2 * rows * cols + rows * cols + scale_bytes
+            gbs = nbytes / (us / 1e6) / 1e9
+            print(json.dumps({
+                "metric": f"{name} GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+                "higher_is_better": True, "dtype": "s8", "data": "synthetic",
+                "config": {"workload": f"{name} [{rows}, {cols}]", "l2": L2_NOTE},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                             "frac": gbs / hbm, "traffic": None, "algorithmic_bytes": nbytes,
+                             "peak_source": f"hbm_gbs, {peak_src} (MEASURED_PEAKS.json)"},
+                "streaming_reference": {"kernel": "torch fp16 -> int8 copy of X",
+                                        "us": round(ref_us, 2),
+                                        "frac_of_hbm": 3 * rows * cols / (ref_us / 1e6) / 1e9 / hbm,
+                                        "ours_vs_reference": ref_us / us}}), flush=True)
+        del Xa, Xz, Qc
+        torch.cuda.empty_cache()
+
+
+def prepass_gbs(w, k_ms: dict, ref_us: dict, peaks: dict) -> dict:
+    """Bandwidth of the two passes before the matmul: the column statistics read X
+    (2 T in bytes); the quantize pass reads X and writes the codes (fp16 for the tensor-core
+    matmul, int8 for the decode kernels) and the row scales. Beside each, the time of a
+    library streaming kernel with the same traffic timed the same way (ref_us)."""
+    hbm = float(peaks["hbm_gbs"])
+    code_bytes = 1 if uses_gemv(w) else 2
+    nb = {"colstats": 2 * w.T * w.d_in,
+          "quantize_gather": 2 * w.T * w.d_in + code_bytes * w.T * w.d_in + 4 * w.T}
+    out = {}
+    for k, b in nb.items():
+        us = statistics.mean(k_ms[k]) * 1e3
+        out[k] = {"us": round(us, 2), "algorithmic_bytes": b, "gbs": b / (us / 1e6) / 1e9,
+                  "frac_of_hbm": b / (us / 1e6) / 1e9 / hbm,
+                  "reference_us": round(ref_us[k], 2), "ours_vs_reference": ref_us[k] / us}
+    return out
 
 
 def main(argv=None) -> None:
@@ -741,6 +791,8 @@ def main(argv=None) -> None:
     ap.add_argument("--all", action="store_true",
                     help="one line per configuration (1 GPU, no CPU baseline)")
     ap.add_argument("--ffn", action="store_true", help="only the FFN block line (1 GPU)")
+    ap.add_argument("--rows", action="store_true",
+                    help="only the standalone quantizer lines (1 GPU)")
     ap.add_argument("--zeropoint", action="store_true",
                     help="zeropoint activation codes (int8_matmul_zeropoint)")
     ap.add_argument("--ffn-workload", default=DEFAULT_FFN, choices=sorted(synth.FFN_WORKLOADS))
@@ -758,6 +810,8 @@ def main(argv=None) -> None:
         run_ours(args)
         args.zeropoint = False
         run_ffn(args)
+        run_rows(args)
+    elif args.rows:
         run_rows(args)
     elif args.ffn:
         if dist_env()[1] > 1:

@@ -12,11 +12,9 @@
 // Vector path (cols % 8 == 0 and block = 8 * g with g a power of two, 2 <= g <= 32): a
 // thread owns one 16-byte chunk (8 values) of a block of g chunks held by g consecutive
 // lanes; the block's absmax is a max over those lanes by shuffles, so no shared memory and
-// no block-wide barrier. Rows are padded to whole blocks of chunk slots (a slot past the row
-// end loads nothing), so groups never straddle rows or warps. Each thread takes kSlots slots
-// spaced one grid apart and issues all their loads before using any (HBM latency is paid
-// once per kSlots chunks), then writes 8 codes (8 bytes) per chunk and, from the group's
-// first lane, the block's absmax. The grid covers the slots in one pass when it can.
+// no block-wide barrier. A warp walks a row kSlots x 32 chunks at a time, issuing all their
+// loads before using any (HBM latency is paid once per kSlots chunks), then writes 8 codes
+// (8 bytes) per chunk and, from the group's first lane, the block's absmax.
 // Other shapes: one thread per block, element by element.
 #include <cuda_fp16.h>
 
@@ -28,7 +26,7 @@ namespace i8mm {
 namespace {
 
 constexpr int kBlkThreads = 256;
-constexpr int kSlots = 4;  // 16-byte chunks in flight per thread
+constexpr int kSlots = 8;  // 16-byte chunks in flight per thread
 
 __device__ __forceinline__ float bh2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
@@ -45,53 +43,61 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
-// G = lanes per block (block = 8 G values).
+// G = lanes per block (block = 8 G values). The work units are segments of 32 x kSlots
+// chunks of a row (a whole number of blocks); warp w of the grid takes units w, w + W, ...
+// In a segment, lane l takes chunks l, l + 32, ..., all loaded before any is used, so the G
+// lanes of a group always hold one block (G divides 32 and a pass starts at a multiple of
+// 32). Chunks past the row end load nothing.
 template <int G>
 __global__ void __launch_bounds__(kBlkThreads) blocks_vec_kernel(
-    const uint16_t* __restrict__ X, int rows, int cols, long long nslots, int slots_per_row,
-    int nblocks, int8_t* __restrict__ Q, float* __restrict__ absmax) {
-  const int cpr = cols >> 3;  // chunks per row
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x; base < nslots;
-       base += stride * kSlots) {
-    uint4 v[kSlots];
-    int row[kSlots], c[kSlots];
+    const uint16_t* __restrict__ X, int rows, int cols, int nblocks, int8_t* __restrict__ Q,
+    float* __restrict__ absmax) {
+  constexpr int kSeg = 32 * kSlots;  // chunks per unit
+  const int cpr = cols >> 3;          // chunks per row
+  const int spr = (cpr + kSeg - 1) / kSeg;
+  const long long units = (long long)rows * spr;
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (kBlkThreads / 32);
+  for (long long un = (long long)blockIdx.x * (kBlkThreads / 32) + (threadIdx.x >> 5);
+       un < units; un += nwarps) {
+    const int row = (int)(un / spr), cb = (int)(un - (long long)row * spr) * kSeg;
+    const uint4* x4 = reinterpret_cast<const uint4*>(X + (size_t)row * cols);
+    uint2* q2 = reinterpret_cast<uint2*>(Q + (size_t)row * cols);
+    float* am = absmax + (size_t)row * nblocks;
+    {
+      uint4 v[kSlots];
 #pragma unroll
-    for (int u = 0; u < kSlots; ++u) {  // all loads first
-      const long long slot = base + stride * u;
-      row[u] = (int)(slot / slots_per_row);
-      c[u] = (int)(slot - (long long)row[u] * slots_per_row);
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (slot < nslots && row[u] < rows && c[u] < cpr)
-        v[u] = ld_stream16(X + (size_t)row[u] * cols + (size_t)c[u] * 8);
-    }
+      for (int u = 0; u < kSlots; ++u) {  // all loads first
+        const int c = cb + 32 * u + lane;
+        v[u] = c < cpr ? ld_stream16(x4 + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int u = 0; u < kSlots; ++u) {
-      const long long slot = base + stride * u;
-      // slot < nslots is the same for the whole warp (nslots is a multiple of 32 slots)
-      if (slot >= nslots) break;
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t m = 0;
+      for (int u = 0; u < kSlots; ++u) {
+        if (cb + 32 * u >= cpr) break;  // uniform: no chunk of this pass is in the row
+        const int c = cb + 32 * u + lane;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t m = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
+        for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
 #pragma unroll
-      for (int d = 1; d < G; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
-      const float a = bh2f((uint16_t)m);
-      const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
-      if (row[u] < rows && c[u] < cpr) {
-        int q[8];
+        for (int d = 1; d < G; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+        const float a = bh2f((uint16_t)m);
+        const float s = a > 0.0f ? __fdiv_rn(127.0f, a) : 0.0f;
+        if (c < cpr) {
+          int q[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          q[2 * k] = blk_code(bh2f((uint16_t)(w[k] & 0xffffu)), s);
-          q[2 * k + 1] = blk_code(bh2f((uint16_t)(w[k] >> 16)), s);
+          for (int k = 0; k < 4; ++k) {
+            q[2 * k] = blk_code(bh2f((uint16_t)(w[k] & 0xffffu)), s);
+            q[2 * k + 1] = blk_code(bh2f((uint16_t)(w[k] >> 16)), s);
+          }
+          uint2 o;
+          o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
+                ((uint32_t)(q[3] & 0xff) << 24);
+          o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
+                ((uint32_t)(q[7] & 0xff) << 24);
+          q2[c] = o;
+          if (c % G == 0) am[c / G] = a;
         }
-        uint2 o;
-        o.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
-              ((uint32_t)(q[3] & 0xff) << 24);
-        o.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) |
-              ((uint32_t)(q[7] & 0xff) << 24);
-        *reinterpret_cast<uint2*>(Q + (size_t)row[u] * cols + (size_t)c[u] * 8) = o;
-        if (c[u] % G == 0) absmax[(size_t)row[u] * nblocks + c[u] / G] = a;
       }
     }
   }
@@ -119,16 +125,12 @@ __global__ void __launch_bounds__(kBlkThreads) blocks_scalar_kernel(
 template <int G>
 cudaError_t launch_vec(const uint16_t* X, int rows, int cols, int8_t* Q, float* absmax,
                        cudaStream_t s) {
-  const int cpr = cols / 8;
-  const int slots_per_row = (cpr + G - 1) / G * G;
-  long long nslots = (long long)rows * slots_per_row;
-  nslots = (nslots + 31) / 32 * 32;  // whole warps (the padding slots load and store nothing)
   const int nblocks = (cols + 8 * G - 1) / (8 * G);
-  // enough threads for every slot in one pass of kSlots, at most 8 CTAs per SM
-  const long long want = (nslots + (long long)kBlkThreads * kSlots - 1) / (kBlkThreads * kSlots);
+  // a warp per unit while units last, at most 8 CTAs of 8 warps per SM
+  const long long units = (long long)rows * ((cols / 8 + 32 * kSlots - 1) / (32 * kSlots));
+  const long long want = (units + kBlkThreads / 32 - 1) / (kBlkThreads / 32);
   const int grid = (int)std::max(1LL, std::min(want, (long long)sm_count() * 8));
-  blocks_vec_kernel<G><<<grid, kBlkThreads, 0, s>>>(X, rows, cols, nslots, slots_per_row,
-                                                    nblocks, Q, absmax);
+  blocks_vec_kernel<G><<<grid, kBlkThreads, 0, s>>>(X, rows, cols, nblocks, Q, absmax);
   return cudaGetLastError();
 }
 
