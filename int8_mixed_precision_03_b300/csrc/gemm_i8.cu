@@ -94,21 +94,32 @@ constexpr bool kDisablePairs = false;
 constexpr uint32_t kWorstChunkBound = 127u * 127u * kChunkK;  // < kExactLimit
 static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact");
 
+// Token tiles up to this size keep the converted weights (A) in TMEM instead of shared
+// memory: the accumulators of a small tile leave room for eight A stages.
+constexpr int kATmemMaxBN = 64;
+
 template <int BN, bool kPair = false>
 struct Cfg {
   static constexpr int kW = 16;  // tokens per epilogue slice
+  // A stages in TMEM (small token tiles): the converters write them with tcgen05.st and the
+  // MMA reads A from TMEM, so shared memory holds only B and the int8 weight ring.
+  static constexpr bool kAT = !kPair && BN <= kATmemMaxBN;
   // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring. A CTA of
   // a pair holds half of the tile's B rows, so its stages are half as large and it affords
   // one more of them.
-  static constexpr int kStages = kPair ? 4 : BN == 256 ? 3 : 4;
-  static constexpr int kStages8 = BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
+  static constexpr int kStages = kAT ? 8 : kPair ? 4 : BN == 256 ? 3 : 4;
+  static constexpr int kStages8 = kAT ? 16 : BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
   static constexpr int kBRows = kPair ? BN / 2 : BN;  // B rows (tokens) in this CTA's stages
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kBoxBytes = kW * 32 * 2;
-  static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN;  // F0 + F1
+  // TMEM: F0 + F1 (2 BN columns), then with kAT the A stages, 32 columns each (128 lanes x
+  // 64 fp16 K values, two per column)
+  static constexpr uint32_t kAcol0 = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr uint32_t kTmemCols = kAT ? 512 : 2 * BN <= 32 ? 32 : 2 * BN;
+  static_assert(!kAT || kAcol0 + 32 * kStages <= 512, "TMEM columns");
   // shared memory (stage bases 1024-byte aligned for the swizzled layouts)
   static constexpr int a16 = 0;
-  static constexpr int b = a16 + kStages * kA16Bytes;
+  static constexpr int b = a16 + (kAT ? 0 : kStages * kA16Bytes);
   static constexpr int a8 = b + kStages * kBBytes;
   static constexpr int box = a8 + kStages8 * kA8Bytes;
   static constexpr int bars = box + 4 * 2 * kBoxBytes;
@@ -555,6 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kPair)
               mma_f16_ss_pair(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
                               (seg_first && k == 0) ? 0u : 1u);
+            else if constexpr (C::kAT)  // A from TMEM: 16 K values = 8 columns per step
+              mma_f16_ts(tmem_base + dcol, tmem_base + C::kAcol0 + 32 * s + 8 * k, bd + 2 * k,
+                         idesc, (seg_first && k == 0) ? 0u : 1u);
             else
               mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
                          (seg_first && k == 0) ? 0u : 1u);
@@ -601,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
           // the MMAs that last read A stage s have completed
           if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
+          if constexpr (C::kAT) tc_fence_after();
           uint32_t a[32];
           if (is_int) {
             const uint32_t s8 = i8_0 % kS8;
@@ -633,14 +648,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
           }
-          const uint32_t dst = sbase + C::a16 + s * kA16Bytes + r * 128;
+          if constexpr (C::kAT) {
+            // row r is TMEM lane r (this warp's quadrant): 32 columns of (even K, odd K)
+            tmem_st<32>(tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kAcol0 + 32 * s, a);
+            tmem_st_wait();
+            tc_fence_before();
+          } else {
+            const uint32_t dst = sbase + C::a16 + s * kA16Bytes + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(dst + (((uint32_t)c ^ swz16) << 4), a[4 * c], a[4 * c + 1],
-                         a[4 * c + 2], a[4 * c + 3]);
-          // each thread orders its shared stores before the tensor core reads them; the
-          // warp then signals once
-          fence_proxy_async_smem();
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(dst + (((uint32_t)c ^ swz16) << 4), a[4 * c], a[4 * c + 1],
+                           a[4 * c + 2], a[4 * c + 3]);
+            // each thread orders its shared stores before the tensor core reads them
+            fence_proxy_async_smem();
+          }
+          // the warp then signals once
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&a8_empty[i8_0 % kS8]);
