@@ -24,7 +24,13 @@
 //       block, copied without conversion.
 //   B = activation codes as fp16 [T, in] (written by the quantize pass), or the outlier
 //       slice X_out fp16 [T, ncap]: TMA, 128-byte swizzle, K-major.
-//   A and B stages form one ring, released by one MMA commit per K block.
+//   A and B stages form one ring, released by one MMA commit per K block. The MMA issuer
+//   waits on one barrier per stage (full_a): a converter warp completes its share of it
+//   only once the stage's B has landed (full_b). Token tiles of at most 64 keep the fp16
+//   A stages in TMEM instead (tcgen05.st by the converters, A-from-TMEM MMAs).
+// For small token tiles an MMA takes about 56 cycles while each barrier query and each
+// step of the issuing thread's own loop takes tens of cycles, so the issuer's loop over a
+// chunk's K blocks does nothing but wait, issue, commit and advance the stage.
 // TMEM: two accumulators F0 [0, BN) and F1 [BN, 2BN) take the segments in turn (the int
 // segments of a tile, then its outlier segment if it has one, then the next tile's), so the
 // epilogue of one segment overlaps the MMAs of the next. The epilogue's running int32 sum of
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- MMA issuer
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = idesc_f16_f32acc(kPair ? 2 * BM : BM, BN);
-      uint32_t it = 0, nseg = 0;
+      uint32_t s = 0, ph = 0, nseg = 0;  // ring stage and its phase; segments issued
       bool ok = true;
       Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
@@ -532,18 +538,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c = c0 - 1;  // current int chunk
         const int kb_lo = c0 * kChunkKBlocks;
         const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
-        for (int kb = kb_lo; kb < kb_end && ok; ++kb, ++it) {
-          // segment boundaries: int chunks grouped by the exactness bound, then the
-          // outlier segment; each segment takes the next accumulator (F0/F1)
-          bool opens = false;
-          if (kb < p.nkb) {
-            if (kb % kChunkKBlocks == 0) {
-              ++c;
-              opens = walker.opens(chunk_bound(p, n_blk, c), c == c0);
-            }
-          } else {
-            opens = kb == p.nkb;
+        for (int kb = kb_lo; kb < kb_end && ok;) {
+          // Segment boundaries, checked once per run of K blocks (the rest of an int chunk,
+          // or the outlier segment): int chunks grouped by the exactness bound, then the
+          // outlier segment; each segment takes the next accumulator (F0/F1).
+          bool opens;
+          int kb_stop;
+          if (kb < p.nkb) {  // kb starts an int chunk
+            ++c;
+            opens = walker.opens(chunk_bound(p, n_blk, c), c == c0);
+            kb_stop = kb + kChunkKBlocks < p.nkb ? kb + kChunkKBlocks : p.nkb;
+          } else {  // kb == p.nkb: the outlier segment
+            opens = true;
+            kb_stop = kb_end;
           }
+          if (kb_stop > kb_end) kb_stop = kb_end;
           if (opens) {
             if (kb > kb_lo) {
               if constexpr (kPair) mma_commit_pair(&tmem_full[nseg & 1u], 3);
@@ -555,27 +564,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             dcol = (nseg & 1u) * BN;
             seg_first = true;
           }
-          const uint32_t s = it % kS, ph = (it / kS) & 1u;
-          if (!(ok = pwait<kPair>(&full_a[s], ph, ab))) break;
-          if (!(ok = pwait<kPair>(&full_b[s], ph, ab))) break;
-          tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
-          const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBBytes);
+          // The run itself does as little as possible per K block: this thread's
+          // instruction stream, not the tensor core, bounds small token tiles. One wait per
+          // stage: a converter arrives on full_a only once the stage's B has landed.
+          for (; kb < kb_stop; ++kb) {
+            if (!(ok = pwait<kPair>(&full_a[s], ph, ab))) break;
+            tc_fence_after();
+            const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBBytes);
+            if constexpr (C::kAT) {  // A from TMEM: 16 K values = 8 columns per step
+              const uint32_t ta = tmem_base + C::kAcol0 + 32 * s;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            if constexpr (kPair)
-              mma_f16_ss_pair(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
-                              (seg_first && k == 0) ? 0u : 1u);
-            else if constexpr (C::kAT)  // A from TMEM: 16 K values = 8 columns per step
-              mma_f16_ts(tmem_base + dcol, tmem_base + C::kAcol0 + 32 * s + 8 * k, bd + 2 * k,
-                         idesc, (seg_first && k == 0) ? 0u : 1u);
-            else
-              mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
-                         (seg_first && k == 0) ? 0u : 1u);
+              for (int k = 0; k < BK / 16; ++k)
+                mma_f16_ts(tmem_base + dcol, ta + 8 * k, bd + 2 * k, idesc,
+                           (seg_first && k == 0) ? 0u : 1u);
+            } else {
+              const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                if constexpr (kPair)
+                  mma_f16_ss_pair(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
+                                  (seg_first && k == 0) ? 0u : 1u);
+                else
+                  mma_f16_ss(tmem_base + dcol, ad + 2 * k, bd + 2 * k, idesc,
+                             (seg_first && k == 0) ? 0u : 1u);
+              }
+            }
+            seg_first = false;
+            if constexpr (kPair) mma_commit_pair(&empty[s], 3);
+            else mma_commit(&empty[s]);
+            if (++s == (uint32_t)kS) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
-          seg_first = false;
-          if constexpr (kPair) mma_commit_pair(&empty[s], 3);
-          else mma_commit(&empty[s]);
         }
         if (!ok) break;
         if constexpr (kPair) mma_commit_pair(&tmem_full[nseg & 1u], 3);
@@ -661,6 +682,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                            a[4 * c + 2], a[4 * c + 3]);
             // each thread orders its shared stores before the tensor core reads them
             fence_proxy_async_smem();
+          }
+          // The stage's B must have landed before the MMA issuer sees full_a complete: warp
+          // 0 of the set waits for it (in a pair, the issuer's full_b counts both halves).
+          if ((warp & 3) == 0 && rank == 0) {
+            if (!(ok = pwait<kPair>(&full_b[s], ph, ab))) break;
           }
           // the warp then signals once
           __syncwarp();
