@@ -113,21 +113,27 @@ struct Cfg {
   // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring. A CTA of
   // a pair holds half of the tile's B rows, so its stages are half as large and it affords
   // one more of them.
-  static constexpr int kStages = kAT ? 8 : kPair ? 4 : BN == 256 ? 3 : 4;
-  static constexpr int kStages8 = kAT ? 16 : BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
+  // K blocks (64 K each) per pipeline stage: two for the A-in-TMEM tiles, whose weight
+  // boxes are then 128 bytes wide (whole 128-byte lines) and whose roles wait, arrive and
+  // commit half as often per weight byte; one otherwise.
+  static constexpr int kKB = kAT ? 2 : 1;
+  static constexpr int kA8Slot = kKB * kA8Bytes;  // one weight-ring slot
+  static constexpr int kStages = kAT ? 6 : kPair ? 4 : BN == 256 ? 3 : 4;
+  static constexpr int kStages8 = kAT ? 6 : BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
   static constexpr int kBRows = kPair ? BN / 2 : BN;  // B rows (tokens) in this CTA's stages
-  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kBBytes = kBRows * BK * 2;     // B of one K block
+  static constexpr int kBStage = kKB * kBBytes;
   static constexpr int kBoxBytes = kW * 32 * 2;
-  // TMEM: F0 + F1 (2 BN columns), then with kAT the A stages, 32 columns each (128 lanes x
-  // 64 fp16 K values, two per column)
+  // TMEM: F0 + F1 (2 BN columns), then with kAT the A stages, 32 columns per K block (128
+  // lanes x 64 fp16 K values, two per column)
   static constexpr uint32_t kAcol0 = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr uint32_t kTmemCols = kAT ? 512 : 2 * BN <= 32 ? 32 : 2 * BN;
-  static_assert(!kAT || kAcol0 + 32 * kStages <= 512, "TMEM columns");
+  static_assert(!kAT || kAcol0 + 32 * kKB * kStages <= 512, "TMEM columns");
   // shared memory (stage bases 1024-byte aligned for the swizzled layouts)
   static constexpr int a16 = 0;
   static constexpr int b = a16 + (kAT ? 0 : kStages * kA16Bytes);
-  static constexpr int a8 = b + kStages * kBBytes;
-  static constexpr int box = a8 + kStages8 * kA8Bytes;
+  static constexpr int a8 = b + kStages * kBStage;
+  static constexpr int box = a8 + kStages8 * kA8Slot;
   static constexpr int bars = box + 4 * 2 * kBoxBytes;
   // full_a, full_b, empty [kStages]; a8_full, a8_empty [kStages8]; tmem_full,
   // tmem_empty [2]; done; epi (the four epilogue warps' rendezvous of split tiles)
@@ -446,7 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool cc = cc_outliers(p, n_out_all);
   const int n_cc = cc ? n_out_all : 0;
   const int nkb_out = cc ? 0 : (n_out_all + 63) / 64;
-  const int nkb_all = p.nkb + nkb_out;
+  // stages of kKB K blocks: a tile's int stages (the last one padded with zeros past K),
+  // then its outlier stages; kChunkSt stages per 1024-K chunk
+  constexpr int kKB = C::kKB;
+  constexpr int kChunkSt = kChunkKBlocks / kKB;
+  const int nst_int = (p.nkb + kKB - 1) / kKB;
+  const int nst_all = nst_int + (nkb_out + kKB - 1) / kKB;
   const uint32_t sbase = smem_u32(smem);
 
   if (warp == kWarpB) {
@@ -460,25 +471,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
         const int n0 = (t % p.n_tiles) * BN + (int)rank * C::kBRows;  // this CTA's B rows
-        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
-        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb, ++it) {
+        const int st_end = c1 == p.nchunks ? nst_all : c1 * kChunkSt;
+        for (int st = c0 * kChunkSt; st < st_end && ok; ++st, ++it) {
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
           if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
-          uint8_t* dst = smem + C::b + s * C::kBBytes;
+          const bool is_int = st < nst_int;
+          // first K (in elements) of the stage in B (activation codes) or X_out
+          const int x0 = (is_int ? st : st - nst_int) * kKB * BK;
           if constexpr (kPair) {
             // both halves complete on the MMA issuer's barrier, which expects both
-            if (rank == 0) mbar_arrive_expect_tx(&full_b[s], 2 * C::kBBytes);
+            if (rank == 0) mbar_arrive_expect_tx(&full_b[s], 2 * C::kBStage);
             const uint32_t bar = mapa_rank(&full_b[s], 0);
-            if (kb < p.nkb)
-              tma_load_2d_pair(dst, &tmB, bar, kb * BK, n0, keep);
-            else
-              tma_load_2d_pair(dst, &tmXo, bar, (kb - p.nkb) * BK, n0, keep);
+            for (int k = 0; k < kKB; ++k) {
+              uint8_t* dst = smem + C::b + s * C::kBStage + k * C::kBBytes;
+              tma_load_2d_pair(dst, is_int ? &tmB : &tmXo, bar, x0 + k * BK, n0, keep);
+            }
           } else {
-            mbar_arrive_expect_tx(&full_b[s], C::kBBytes);
-            if (kb < p.nkb)
-              tma_load_2d_hint(dst, &tmB, &full_b[s], kb * BK, n0, keep);
-            else
-              tma_load_2d(dst, &tmXo, &full_b[s], (kb - p.nkb) * BK, n0);
+            mbar_arrive_expect_tx(&full_b[s], C::kBStage);
+            for (int k = 0; k < kKB; ++k) {
+              uint8_t* dst = smem + C::b + s * C::kBStage + k * C::kBBytes;
+              if (is_int)
+                tma_load_2d_hint(dst, &tmB, &full_b[s], x0 + k * BK, n0, keep);
+              else
+                tma_load_2d(dst, &tmXo, &full_b[s], x0 + k * BK, n0);
+            }
           }
         }
       }
@@ -494,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpA8) {
     // -------------------------------------------------------- TMA: weight stream
-    // One 128 x 64 int8 box per int K block; two 128 x 32 fp16 boxes per outlier K block.
+    // One 128 x 64 kKB int8 box per int stage; two 128 x 32 kKB fp16 boxes per outlier stage.
     if (lane == 0 && !p.debug_skip_loads) {
       uint32_t i8 = 0;
       bool ok = true;
@@ -502,18 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
         const int m0 = (t / p.n_tiles) * kFeatTile + (int)rank * BM;
-        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
-        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb) {
-          const int nbox = kb < p.nkb ? 1 : 2;
+        const int st_end = c1 == p.nchunks ? nst_all : c1 * kChunkSt;
+        for (int st = c0 * kChunkSt; st < st_end && ok; ++st) {
+          const bool is_int = st < nst_int;
+          const int nbox = is_int ? 1 : 2;
           for (int h = 0; h < nbox && ok; ++h, ++i8) {
             const uint32_t s8 = i8 % kS8, ph8 = (i8 / kS8) & 1u;
             if (!(ok = pipe_wait(&a8_empty[s8], ph8 ^ 1u, ab))) break;
-            mbar_arrive_expect_tx(&a8_full[s8], kA8Bytes);
-            uint8_t* dst = smem + C::a8 + s8 * kA8Bytes;
-            if (kb < p.nkb)
-              tma_load_2d(dst, &tmA8, &a8_full[s8], kb * BK, m0);
+            mbar_arrive_expect_tx(&a8_full[s8], C::kA8Slot);
+            uint8_t* dst = smem + C::a8 + s8 * C::kA8Slot;
+            if (is_int)
+              tma_load_2d(dst, &tmA8, &a8_full[s8], st * kKB * BK, m0);
             else
-              tma_load_2d(dst, &tmWo, &a8_full[s8], (kb - p.nkb) * BK + 32 * h, m0);
+              tma_load_2d(dst, &tmWo, &a8_full[s8], (st - nst_int) * kKB * BK + 32 * kKB * h,
+                          m0);
           }
         }
       }
@@ -536,25 +554,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool seg_first = true;
         uint32_t dcol = 0;
         int c = c0 - 1;  // current int chunk
-        const int kb_lo = c0 * kChunkKBlocks;
-        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
-        for (int kb = kb_lo; kb < kb_end && ok;) {
-          // Segment boundaries, checked once per run of K blocks (the rest of an int chunk,
+        const int st_lo = c0 * kChunkSt;
+        const int st_end = c1 == p.nchunks ? nst_all : c1 * kChunkSt;
+        for (int st = st_lo; st < st_end && ok;) {
+          // Segment boundaries, checked once per run of stages (the rest of an int chunk,
           // or the outlier segment): int chunks grouped by the exactness bound, then the
           // outlier segment; each segment takes the next accumulator (F0/F1).
           bool opens;
-          int kb_stop;
-          if (kb < p.nkb) {  // kb starts an int chunk
+          int st_stop;
+          if (st < nst_int) {  // st starts an int chunk
             ++c;
             opens = walker.opens(chunk_bound(p, n_blk, c), c == c0);
-            kb_stop = kb + kChunkKBlocks < p.nkb ? kb + kChunkKBlocks : p.nkb;
-          } else {  // kb == p.nkb: the outlier segment
+            st_stop = st + kChunkSt < nst_int ? st + kChunkSt : nst_int;
+          } else {  // st == nst_int: the outlier segment
             opens = true;
-            kb_stop = kb_end;
+            st_stop = st_end;
           }
-          if (kb_stop > kb_end) kb_stop = kb_end;
+          if (st_stop > st_end) st_stop = st_end;
           if (opens) {
-            if (kb > kb_lo) {
+            if (st > st_lo) {
               if constexpr (kPair) mma_commit_pair(&tmem_full[nseg & 1u], 3);
               else mma_commit(&tmem_full[nseg & 1u]);
               ++nseg;
@@ -567,16 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The run itself does as little as possible per K block: this thread's
           // instruction stream, not the tensor core, bounds small token tiles. One wait per
           // stage: a converter arrives on full_a only once the stage's B has landed.
-          for (; kb < kb_stop; ++kb) {
+          for (; st < st_stop; ++st) {
             if (!(ok = pwait<kPair>(&full_a[s], ph, ab))) break;
             tc_fence_after();
-            const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBBytes);
+            const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBStage);
             if constexpr (C::kAT) {  // A from TMEM: 16 K values = 8 columns per step
-              const uint32_t ta = tmem_base + C::kAcol0 + 32 * s;
+              const uint32_t ta = tmem_base + C::kAcol0 + 32 * kKB * s;
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k)
-                mma_f16_ts(tmem_base + dcol, ta + 8 * k, bd + 2 * k, idesc,
-                           (seg_first && k == 0) ? 0u : 1u);
+              for (int j = 0; j < kKB; ++j) {  // K block j of the stage
+                const uint64_t bdj = bd + (uint64_t)((j * C::kBBytes) >> 4);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                  mma_f16_ts(tmem_base + dcol, ta + 32 * j + 8 * k, bdj + 2 * k, idesc,
+                             (seg_first && j == 0 && k == 0) ? 0u : 1u);
+              }
             } else {
               const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
 #pragma unroll
@@ -612,41 +634,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if ((warp >= kWarpConv0 && warp < kWarpConv0 + 4) || warp >= kWarpConv1) {
     // -------------------------------------------------------- weights into fp16 A
-    // Thread `lane` of warp q of a set handles row r = 32q + lane of each 128 x 64 A block:
-    // 16-byte loads from the weight ring (64-byte TMA swizzle: chunk c of row r sits at
-    // chunk c ^ ((r >> 1) & 3)), int8 -> fp16 in registers (fp16 outlier weights are
-    // copied as they are), eight 16-byte stores into the 128-byte-swizzled A stage
-    // (chunk c of row r at chunk c ^ (r & 7)).
+    // Thread `lane` of warp q of a set handles row r = 32q + lane of each stage's 128 x 64 kKB
+    // A block: 16-byte loads from the weight ring (TMA swizzle of the slot's row width: 64
+    // bytes, chunk c of row r at chunk c ^ ((r >> 1) & 3); 128 bytes, at c ^ (r & 7)), int8
+    // -> fp16 in registers (fp16 outlier weights are copied as they are), then either TMEM
+    // stores (kAT) or eight 16-byte stores into the 128-byte-swizzled A stage in shared
+    // memory (chunk c of row r at chunk c ^ (r & 7)).
     if (!p.debug_skip_loads) {
       const int set = warp >= kWarpConv1 ? 1 : 0;
       const int r = 32 * (warp & 3) + lane;
-      const uint32_t swz8 = (uint32_t)(r >> 1) & 3u;
+      const uint32_t swz8 = kKB == 2 ? (uint32_t)r & 7u : (uint32_t)(r >> 1) & 3u;
       const uint32_t swz16 = (uint32_t)r & 7u;
       uint32_t it = 0, i8 = 0;
       bool ok = true;
       Sched<kSplit, kPair> sc(p);
       int t, c0, c1;
       while (ok && sc.next(p, t, c0, c1)) {
-        const int kb_end = c1 == p.nchunks ? nkb_all : c1 * kChunkKBlocks;
-        for (int kb = c0 * kChunkKBlocks; kb < kb_end && ok; ++kb, ++it) {
-          const bool is_int = kb < p.nkb;
+        const int st_end = c1 == p.nchunks ? nst_all : c1 * kChunkSt;
+        for (int st = c0 * kChunkSt; st < st_end && ok; ++st, ++it) {
+          const bool is_int = st < nst_int;
           const uint32_t i8_0 = i8;
           i8 += is_int ? 1u : 2u;
-          if ((int)(it & 1u) != set) continue;  // K block `it` belongs to set it & 1
+          if ((int)(it & 1u) != set) continue;  // stage `it` belongs to set it & 1
           const uint32_t s = it % kS, ph = (it / kS) & 1u;
           // the MMAs that last read A stage s have completed
           if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
           if constexpr (C::kAT) tc_fence_after();
-          uint32_t a[32];
+          uint32_t a[32 * kKB];  // K block j of the stage in a[32 j .. 32 j + 31]
           if (is_int) {
             const uint32_t s8 = i8_0 % kS8;
             if (!(ok = pwait<kPair>(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
-            const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
-            uint4 v[4];
+            const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64 * kKB;
+            uint4 v[4 * kKB];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
+            for (int c = 0; c < 4 * kKB; ++c)
+              v[c] = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 4 * kKB; ++c) {
               uint32_t o[8];
               cvt_s8x16_to_f16x16(v[c], o);
 #pragma unroll
@@ -654,27 +678,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {  // slot h: fp16 columns [32 kKB h, 32 kKB (h + 1))
               const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
               if (!(ok = pwait<kPair>(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
-              const uint32_t src = sbase + C::a8 + s8 * kA8Bytes + r * 64;
+              const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64 * kKB;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < 4 * kKB; ++c) {
                 const uint4 v = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
-                a[16 * h + 4 * c + 0] = v.x;
-                a[16 * h + 4 * c + 1] = v.y;
-                a[16 * h + 4 * c + 2] = v.z;
-                a[16 * h + 4 * c + 3] = v.w;
+                a[16 * kKB * h + 4 * c + 0] = v.x;
+                a[16 * kKB * h + 4 * c + 1] = v.y;
+                a[16 * kKB * h + 4 * c + 2] = v.z;
+                a[16 * kKB * h + 4 * c + 3] = v.w;
               }
             }
             if (!ok) break;
           }
           if constexpr (C::kAT) {
-            // row r is TMEM lane r (this warp's quadrant): 32 columns of (even K, odd K)
-            tmem_st<32>(tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kAcol0 + 32 * s, a);
+            // row r is TMEM lane r (this warp's quadrant): 32 columns of (even K, odd K) per
+            // K block
+            const uint32_t ta =
+                tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kAcol0 + 32 * kKB * s;
+#pragma unroll
+            for (int j = 0; j < kKB; ++j)
+              tmem_st<32>(ta + 32 * j, *reinterpret_cast<const uint32_t(*)[32]>(a + 32 * j));
             tmem_st_wait();
             tc_fence_before();
           } else {
+            static_assert(C::kKB == 1, "shared-memory A stages hold one K block");
             const uint32_t dst = sbase + C::a16 + s * kA16Bytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -1202,13 +1232,17 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<BN>;
   CUtensorMap mA8, mB, mWo, mXo, mY;
   bool ok = true;
-  ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM, BK,
-                 CU_TENSOR_MAP_SWIZZLE_64B);
+  // weight boxes: 128 rows x one stage of K (64 or 128 bytes), swizzled across the row
+  const CUtensorMapSwizzle sw8 =
+      C::kKB == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM, BK * C::kKB,
+                 sw8);
   ok &= make_map(&mB, a.b_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.in, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
-  // outlier weights: 128 rows x 32 fp16 (64 bytes) per box, two boxes per K block
-  ok &= make_map(&mWo, a.wout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out, a.ncap, BM, BK / 2,
-                 CU_TENSOR_MAP_SWIZZLE_64B);
+  // outlier weights: 128 rows x 32 kKB fp16 (the same bytes as a weight box), two boxes per
+  // stage
+  ok &= make_map(&mWo, a.wout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out, a.ncap, BM,
+                 BK / 2 * C::kKB, sw8);
   ok &= make_map(&mXo, a.xout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.ncap, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   // Y [T, out] fp16 through TMA stores when its row pitch is a multiple of 16 bytes
