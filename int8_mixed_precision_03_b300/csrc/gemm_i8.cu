@@ -103,6 +103,12 @@ static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact")
 // Token tiles up to this size keep the converted weights (A) in TMEM instead of shared
 // memory: the accumulators of a small tile leave room for eight A stages.
 constexpr int kATmemMaxBN = 64;
+// K blocks per stage of those tiles (2 or 4; with 4, three stages fill TMEM). Measured on
+// the 176B decode shape (64 tokens x 14336 -> 57344): one K block 264 us, two 209 us, four
+// 191 us.
+constexpr int kATKBlocks = 4;
+// a 128-row x 128-byte weight box in shared memory
+constexpr int kBox8Bytes = 128 * 128;
 
 template <int BN, bool kPair = false>
 struct Cfg {
@@ -113,13 +119,15 @@ struct Cfg {
   // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring. A CTA of
   // a pair holds half of the tile's B rows, so its stages are half as large and it affords
   // one more of them.
-  // K blocks (64 K each) per pipeline stage: two for the A-in-TMEM tiles, whose weight
-  // boxes are then 128 bytes wide (whole 128-byte lines) and whose roles wait, arrive and
-  // commit half as often per weight byte; one otherwise.
-  static constexpr int kKB = kAT ? 2 : 1;
-  static constexpr int kA8Slot = kKB * kA8Bytes;  // one weight-ring slot
-  static constexpr int kStages = kAT ? 6 : kPair ? 4 : BN == 256 ? 3 : 4;
-  static constexpr int kStages8 = kAT ? 6 : BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
+  // K blocks (64 K each) per pipeline stage: kATKBlocks for the A-in-TMEM tiles, whose
+  // weight boxes are then 128 bytes wide (whole 128-byte lines) and whose roles wait, arrive
+  // and commit once per 16 or 32 KB of weights; one otherwise.
+  static constexpr int kKB = kAT ? kATKBlocks : 1;
+  static constexpr int kA8Slot = kKB * kA8Bytes;       // one weight-ring slot
+  static constexpr int kBoxKB = kKB >= 2 ? 2 : 1;      // K blocks per weight box
+  static constexpr int kSub = kKB / kBoxKB;            // weight boxes per slot
+  static constexpr int kStages = kAT ? 12 / kKB : kPair ? 4 : BN == 256 ? 3 : 4;
+  static constexpr int kStages8 = kAT ? 12 / kKB : BN == 256 ? 8 : BN == 128 ? 6 : BN == 64 ? 10 : 12;
   static constexpr int kBRows = kPair ? BN / 2 : BN;  // B rows (tokens) in this CTA's stages
   static constexpr int kBBytes = kBRows * BK * 2;     // B of one K block
   static constexpr int kBStage = kKB * kBBytes;
@@ -526,12 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t s8 = i8 % kS8, ph8 = (i8 / kS8) & 1u;
             if (!(ok = pipe_wait(&a8_empty[s8], ph8 ^ 1u, ab))) break;
             mbar_arrive_expect_tx(&a8_full[s8], C::kA8Slot);
-            uint8_t* dst = smem + C::a8 + s8 * C::kA8Slot;
-            if (is_int)
-              tma_load_2d(dst, &tmA8, &a8_full[s8], st * kKB * BK, m0);
-            else
-              tma_load_2d(dst, &tmWo, &a8_full[s8], (st - nst_int) * kKB * BK + 32 * kKB * h,
-                          m0);
+#pragma unroll
+            for (int b = 0; b < C::kSub; ++b) {  // boxes of 64 kBoxKB bytes side by side in K
+              uint8_t* dst = smem + C::a8 + s8 * C::kA8Slot + b * (C::kA8Slot / C::kSub);
+              if (is_int)
+                tma_load_2d(dst, &tmA8, &a8_full[s8], (st * kKB + b * C::kBoxKB) * BK, m0);
+              else
+                tma_load_2d(dst, &tmWo, &a8_full[s8],
+                            (st - nst_int) * kKB * BK + 32 * kKB * h + 32 * C::kBoxKB * b, m0);
+            }
           }
         }
       }
@@ -591,8 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sdesc_kmajor_sw128(sbase + C::b + s * C::kBStage);
             if constexpr (C::kAT) {  // A from TMEM: 16 K values = 8 columns per step
               const uint32_t ta = tmem_base + C::kAcol0 + 32 * kKB * s;
+              // K blocks of the stage that hold data: past K the int boxes read zeros (outside
+              // the tensors), but the outlier slices are zero-padded only to a multiple of 64
+              // columns, so an outlier stage stops at its last K block
+              const int nvalid = st < nst_int ? kKB : nkb_out - (st - nst_int) * kKB;
 #pragma unroll
               for (int j = 0; j < kKB; ++j) {  // K block j of the stage
+                if (j >= nvalid) break;
                 const uint64_t bdj = bd + (uint64_t)((j * C::kBBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
@@ -643,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!p.debug_skip_loads) {
       const int set = warp >= kWarpConv1 ? 1 : 0;
       const int r = 32 * (warp & 3) + lane;
-      const uint32_t swz8 = kKB == 2 ? (uint32_t)r & 7u : (uint32_t)(r >> 1) & 3u;
+      const uint32_t swz8 = (uint32_t)(r >> 1) & 3u;  // 64-byte-wide boxes (kKB = 1)
       const uint32_t swz16 = (uint32_t)r & 7u;
       uint32_t it = 0, i8 = 0;
       bool ok = true;
@@ -660,51 +676,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the MMAs that last read A stage s have completed
           if (!(ok = pwait<kPair>(&empty[s], ph ^ 1u, ab))) break;
           if constexpr (C::kAT) tc_fence_after();
-          uint32_t a[32 * kKB];  // K block j of the stage in a[32 j .. 32 j + 31]
-          if (is_int) {
-            const uint32_t s8 = i8_0 % kS8;
-            if (!(ok = pwait<kPair>(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
-            const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64 * kKB;
-            uint4 v[4 * kKB];
-#pragma unroll
-            for (int c = 0; c < 4 * kKB; ++c)
-              v[c] = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
-#pragma unroll
-            for (int c = 0; c < 4 * kKB; ++c) {
-              uint32_t o[8];
-              cvt_s8x16_to_f16x16(v[c], o);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) a[8 * c + k] = o[k];
-            }
-          } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {  // slot h: fp16 columns [32 kKB h, 32 kKB (h + 1))
-              const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
-              if (!(ok = pwait<kPair>(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
-              const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64 * kKB;
-#pragma unroll
-              for (int c = 0; c < 4 * kKB; ++c) {
-                const uint4 v = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
-                a[16 * kKB * h + 4 * c + 0] = v.x;
-                a[16 * kKB * h + 4 * c + 1] = v.y;
-                a[16 * kKB * h + 4 * c + 2] = v.z;
-                a[16 * kKB * h + 4 * c + 3] = v.w;
-              }
-            }
-            if (!ok) break;
-          }
           if constexpr (C::kAT) {
-            // row r is TMEM lane r (this warp's quadrant): 32 columns of (even K, odd K) per
-            // K block
+            // One K block at a time from the slot's 128-byte-wide boxes (128 rows x 128
+            // bytes, 128-byte swizzle: chunk c of row r at c ^ (r & 7)): an int box holds two
+            // K blocks, an fp16 outlier box one. Converted (int) or copied (fp16), then
+            // stored to TMEM lane r: 32 columns of (even K, odd K) per K block.
             const uint32_t ta =
                 tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + C::kAcol0 + 32 * kKB * s;
+            uint32_t held = ~0u;  // the slot whose barrier this thread has waited on
 #pragma unroll
-            for (int j = 0; j < kKB; ++j)
-              tmem_st<32>(ta + 32 * j, *reinterpret_cast<const uint32_t(*)[32]>(a + 32 * j));
+            for (int j = 0; j < kKB; ++j) {
+              const uint32_t h = is_int ? 0u : (uint32_t)(2 * j / kKB);  // slot of the stage
+              const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
+              if (j8 != held) {
+                if (!(ok = pwait<kPair>(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
+                held = j8;
+              }
+              const uint32_t box = is_int ? (uint32_t)j / 2 : (uint32_t)(j - (int)h * kKB / 2);
+              const uint32_t row = sbase + C::a8 + s8 * C::kA8Slot + box * kBox8Bytes + r * 128;
+              uint32_t a[32];
+              if (is_int) {
+                const uint32_t cb = 4u * (uint32_t)(j % 2);
+                uint4 v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  v[c] = ld_shared_v4(row + ((((uint32_t)c + cb) ^ swz16) << 4));
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  uint32_t o[8];
+                  cvt_s8x16_to_f16x16(v[c], o);
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) a[8 * c + k] = o[k];
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint4 v = ld_shared_v4(row + (((uint32_t)c ^ swz16) << 4));
+                  a[4 * c + 0] = v.x;
+                  a[4 * c + 1] = v.y;
+                  a[4 * c + 2] = v.z;
+                  a[4 * c + 3] = v.w;
+                }
+              }
+              tmem_st<32>(ta + 32 * j, a);
+            }
+            if (!ok) break;
             tmem_st_wait();
             tc_fence_before();
           } else {
             static_assert(C::kKB == 1, "shared-memory A stages hold one K block");
+            uint32_t a[32];
+            if (is_int) {
+              const uint32_t s8 = i8_0 % kS8;
+              if (!(ok = pwait<kPair>(&a8_full[s8], (i8_0 / kS8) & 1u, ab))) break;
+              const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64;
+              uint4 v[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) v[c] = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t o[8];
+                cvt_s8x16_to_f16x16(v[c], o);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) a[8 * c + k] = o[k];
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {  // slot h: fp16 columns [32 h, 32 h + 32)
+                const uint32_t j8 = i8_0 + h, s8 = j8 % kS8;
+                if (!(ok = pwait<kPair>(&a8_full[s8], (j8 / kS8) & 1u, ab))) break;
+                const uint32_t src = sbase + C::a8 + s8 * C::kA8Slot + r * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const uint4 v = ld_shared_v4(src + (((uint32_t)c ^ swz8) << 4));
+                  a[16 * h + 4 * c + 0] = v.x;
+                  a[16 * h + 4 * c + 1] = v.y;
+                  a[16 * h + 4 * c + 2] = v.z;
+                  a[16 * h + 4 * c + 3] = v.w;
+                }
+              }
+              if (!ok) break;
+            }
             const uint32_t dst = sbase + C::a16 + s * kA16Bytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -1234,15 +1286,15 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t s) {
   bool ok = true;
   // weight boxes: 128 rows x one stage of K (64 or 128 bytes), swizzled across the row
   const CUtensorMapSwizzle sw8 =
-      C::kKB == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM, BK * C::kKB,
-                 sw8);
+      C::kBoxKB == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  ok &= make_map(&mA8, a.a_int8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.out, a.in, BM,
+                 BK * C::kBoxKB, sw8);
   ok &= make_map(&mB, a.b_f16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.in, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   // outlier weights: 128 rows x 32 kKB fp16 (the same bytes as a weight box), two boxes per
   // stage
   ok &= make_map(&mWo, a.wout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out, a.ncap, BM,
-                 BK / 2 * C::kKB, sw8);
+                 BK / 2 * C::kBoxKB, sw8);
   ok &= make_map(&mXo, a.xout, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.T, a.ncap, b_rows, BK,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   // Y [T, out] fp16 through TMA stores when its row pitch is a multiple of 16 bytes

@@ -116,6 +116,9 @@ def test_tiny_config(i8):
     (1, 16, 1, 0), (2, 48, 7, 1), (7, 64, 129, 3), (8, 128, 100, 15), (9, 256, 257, 16),
     (63, 1040, 300, 17), (64, 2064, 128, 65), (65, 512, 384, 0), (129, 1024, 520, 5),
     (300, 3072, 640, 40), (257, 4096, 255, 2),
+    # small token tiles (stages of four K blocks): a partial last int stage and outlier
+    # counts whose last outlier stage is partly past the zero-padded slices
+    (48, 1040, 272, 40), (17, 1536, 200, 100), (33, 4160, 136, 33),
 ])
 def test_ragged_shapes(i8, T, d, out, k):
     w = synth.Workload("ragged", T, d, out, n_outlier_cols=k, row_frac=0.7, seed=T * 7 + d)
