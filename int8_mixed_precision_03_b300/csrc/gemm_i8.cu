@@ -606,14 +606,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the tensors), but the outlier slices are zero-padded only to a multiple of 64
               // columns, so an outlier stage stops at its last K block
               const int nvalid = st < nst_int ? kKB : nkb_out - (st - nst_int) * kKB;
-#pragma unroll
-              for (int j = 0; j < kKB; ++j) {  // K block j of the stage
-                if (j >= nvalid) break;
+              // the MMAs of K block j of the stage
+              auto kblock = [&](int j) {
                 const uint64_t bdj = bd + (uint64_t)((j * C::kBBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
                   mma_f16_ts(tmem_base + dcol, ta + 32 * j + 8 * k, bdj + 2 * k, idesc,
                              (seg_first && j == 0 && k == 0) ? 0u : 1u);
+              };
+              if (nvalid >= kKB) {
+                // a whole stage (every int stage): one straight run of MMAs, no test
+                // between them (a test inside the unrolled run cost 6-10 % at 16-64 tokens)
+#pragma unroll
+                for (int j = 0; j < kKB; ++j) kblock(j);
+              } else {
+                for (int j = 0; j < nvalid; ++j) kblock(j);
               }
             } else {
               const uint64_t ad = sdesc_kmajor_sw128(sbase + C::a16 + s * kA16Bytes);
