@@ -16,21 +16,24 @@
 // <= 2^24; a single chunk always fits (127 * 127 * 1024 < 2^24). At a segment boundary the
 // epilogue converts the fp32 tile to int32 and adds it to a running int32 sum.
 //
-// Tile: M = 128 output features (TMEM lanes) x N = BN tokens (TMEM columns), K stage 64.
-//   A = CB int8 [out, in]: streamed by TMA (64-byte swizzle) into a deep int8 ring; two
-//       sets of four converter warps (alternate K blocks) turn each 128 x 64 block into
-//       fp16 in the 128-byte-swizzled K-major layout in shared memory. The outlier weight
-//       slice W_out fp16 [out, ncap] takes the same route as two 64-byte-wide boxes per K
-//       block, copied without conversion.
+// Tile: M = 128 output features (TMEM lanes) x N = BN tokens (TMEM columns); a pipeline
+// stage is one 64-K block, or four for token tiles of at most 64 (below).
+//   A = CB int8 [out, in]: streamed by TMA into a weight ring of its own (64-byte-wide boxes
+//       with the 64-byte swizzle; 128-byte-wide boxes with the 128-byte swizzle when a stage
+//       holds several K blocks); two sets of four converter warps (alternate stages) turn
+//       each 128 x 64 block into fp16, stored in the 128-byte-swizzled K-major layout in
+//       shared memory, or, for token tiles of at most 64, into TMEM (tcgen05.st; the MMAs
+//       then read A from TMEM). The outlier weight slice W_out fp16 [out, ncap] takes the
+//       same route as two boxes per stage, copied without conversion.
 //   B = activation codes as fp16 [T, in] (written by the quantize pass), or the outlier
-//       slice X_out fp16 [T, ncap]: TMA, 128-byte swizzle, K-major.
-//   A and B stages form one ring, released by one MMA commit per K block. The MMA issuer
+//       slice X_out fp16 [T, ncap]: TMA, 128-byte swizzle, K-major, one box per K block.
+//   A and B stages form one ring, released by one MMA commit per stage. The MMA issuer
 //   waits on one barrier per stage (full_a): a converter warp completes its share of it
-//   only once the stage's B has landed (full_b). Token tiles of at most 64 keep the fp16
-//   A stages in TMEM instead (tcgen05.st by the converters, A-from-TMEM MMAs).
+//   only once the stage's B has landed (full_b).
 // For small token tiles an MMA takes about 56 cycles while each barrier query and each
-// step of the issuing thread's own loop takes tens of cycles, so the issuer's loop over a
-// chunk's K blocks does nothing but wait, issue, commit and advance the stage.
+// step of the issuing thread's own loop takes tens of cycles, so stages hold four K blocks
+// (16 MMAs) there, and the issuer's loop over a chunk's stages does nothing but wait, issue,
+// commit and advance the stage.
 // TMEM: two accumulators F0 [0, BN) and F1 [BN, 2BN) take the segments in turn (the int
 // segments of a tile, then its outlier segment if it has one, then the next tile's), so the
 // epilogue of one segment overlaps the MMAs of the next. The epilogue's running int32 sum of
