@@ -104,7 +104,7 @@ constexpr uint32_t kWorstChunkBound = 127u * 127u * kChunkK;  // < kExactLimit
 static_assert(kWorstChunkBound <= kExactLimit, "one chunk must always be exact");
 
 // Token tiles up to this size keep the converted weights (A) in TMEM instead of shared
-// memory: the accumulators of a small tile leave room for eight A stages.
+// memory: the two accumulators of a small tile leave room for the A stages.
 constexpr int kATmemMaxBN = 64;
 // K blocks per stage of those tiles (2 or 4; with 4, three stages fill TMEM). Measured on
 // the 176B decode shape (64 tokens x 14336 -> 57344): one K block 264 us, two 209 us, four
@@ -119,12 +119,13 @@ struct Cfg {
   // A stages in TMEM (small token tiles): the converters write them with tcgen05.st and the
   // MMA reads A from TMEM, so shared memory holds only B and the int8 weight ring.
   static constexpr bool kAT = !kPair && BN <= kATmemMaxBN;
-  // ring depths: A (fp16) + B in one ring, the int8 weight stream in its own ring. A CTA of
-  // a pair holds half of the tile's B rows, so its stages are half as large and it affords
-  // one more of them.
   // K blocks (64 K each) per pipeline stage: kATKBlocks for the A-in-TMEM tiles, whose
   // weight boxes are then 128 bytes wide (whole 128-byte lines) and whose roles wait, arrive
   // and commit once per 16 or 32 KB of weights; one otherwise.
+  // Ring depths (kStages, kStages8): A (fp16, in TMEM or shared memory) + B in one ring of
+  // stages, the int8 weight stream in its own ring of slots; with A in TMEM both hold 12 K
+  // blocks. A CTA of a pair holds half of the tile's B rows, so its stages are half as large
+  // and it affords one more of them.
   static constexpr int kKB = kAT ? kATKBlocks : 1;
   static constexpr int kA8Slot = kKB * kA8Bytes;       // one weight-ring slot
   static constexpr int kBoxKB = kKB >= 2 ? 2 : 1;      // K blocks per weight box
