@@ -242,7 +242,8 @@ def test_workspace_reuse_across_calls(i8):
 
 
 # ----------------------------------------------------------------- standalone quantizers
-@pytest.mark.parametrize("rows,cols", [(1024, 8192), (3, 7), (5, 1000), (17, 40), (2, 1)])
+@pytest.mark.parametrize("rows,cols", [(1024, 8192), (16384, 8192), (3, 7), (5, 1000),
+                                       (17, 40), (2, 1)])
 def test_absmax_rows_bit_exact(i8, rows, cols):
     X = synth.make_random_f16(rows * 31 + cols, (rows, cols), std=1.5)
     X[0, :] = 0
@@ -254,6 +255,7 @@ def test_absmax_rows_bit_exact(i8, rows, cols):
 
 @pytest.mark.parametrize("rows,cols,block", [
     (1024, 8192, 64), (1024, 8192, 128),      # the sweep's X, the pages' block sizes
+    (16384, 8192, 64),                         # the bench's large input
     (37, 1000, 64),                            # ragged last block (1000 = 15 * 64 + 40)
     (5, 200, 16), (3, 4104, 256), (9, 520, 32),
     (7, 100, 64),                              # cols % 8 != 0 (element path)
@@ -270,7 +272,7 @@ def test_absmax_blocks_bit_exact(i8, rows, cols, block):
     np.testing.assert_array_equal(a.cpu().numpy(), ao)
 
 
-@pytest.mark.parametrize("rows,cols", [(1024, 8192), (4, 9), (6, 1000), (3, 1)])
+@pytest.mark.parametrize("rows,cols", [(1024, 8192), (16384, 8192), (4, 9), (6, 1000), (3, 1)])
 def test_zeropoint_rows_bit_exact(i8, rows, cols):
     w = synth.Workload("zp", rows, cols, 1)
     X = synth.make_relu_like(w)
