@@ -113,6 +113,13 @@ constexpr int kATKBlocks = 4;
 // a 128-row x 128-byte weight box in shared memory
 constexpr int kBox8Bytes = 128 * 128;
 
+// Selects the zeropoint epilogue's 64-bit form (true) or its int32 form (false) at compile
+// time, so that a slice's loop carries only one of them.
+template <bool B>
+struct Wide {
+  static constexpr bool value = B;
+};
+
 template <int BN, bool kPair = false>
 struct Cfg {
   static constexpr int kW = 16;  // tokens per epilogue slice
@@ -893,43 +900,50 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               const float ra_s = ra[0];  // this slice's tokens, one per lane
               [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
+              // zeropoint: the int32 form is exact for all 32 tokens of the group (uniform)
+              [[maybe_unused]] const bool z32 =
+                  kZp && __all_sync(0xffffffffu, abs(za_s) <= p.z_safe);
               uint32_t yh[kW / 2];
+              auto slice_y = [&](auto wide) {
   #pragma unroll
-              for (int j = 0; j < kW; ++j) {
-                int acc;
-                float fo = fcc[j];
-                if (is_out) {
-                  acc = pc[j];
-                  fo = __uint_as_float(f[j]);
-                } else {
-                  acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
-                }
-                const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
-                float y;
-                if constexpr (kZp) {
-                  // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
-                  // when |Z| <= z_safe bounds it below 2^31 (token j is the same for the
-                  // whole warp, so the branch is uniform), in 64 bits otherwise
-                  const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
-                  if (abs(zj) <= p.z_safe) {
-                    y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
+                for (int j = 0; j < kW; ++j) {
+                  int acc;
+                  float fo = fcc[j];
+                  if (is_out) {
+                    acc = pc[j];
+                    fo = __uint_as_float(f[j]);
                   } else {
-                    const long long az = (long long)acc + (long long)zj * (long long)cbin;
-                    y = __ll2float_rn(az) * (rj * so) + fo + bo;
+                    acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
                   }
-                } else {
-                  y = (float)acc * (rj * so) + fo + bo;
+                  const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+                  float y;
+                  if constexpr (kZp) {
+                    // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
+                    // when |Z| <= z_safe bounds it below 2^31, in 64 bits otherwise
+                    const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
+                    if constexpr (decltype(wide)::value) {
+                      const long long az = (long long)acc + (long long)zj * (long long)cbin;
+                      y = __fmaf_rn(__ll2float_rn(az), rj * so, fo) + bo;
+                    } else {
+                      y = __fmaf_rn((float)(acc + zj * cbin), rj * so, fo) + bo;
+                    }
+                  } else {
+                    y = __fmaf_rn((float)acc, rj * so, fo) + bo;
+                  }
+                  if constexpr (kNext) {
+                    if (p.next_relu) y = fmaxf(y, 0.0f);
+                  }
+                  const uint32_t h = __half_as_ushort(__float2half_rn(y));
+                  if constexpr (kNext) {
+                    if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
+                  }
+                  yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
+                  if constexpr (kDebug) pc[j] = acc;
                 }
-                if constexpr (kNext) {
-                  if (p.next_relu) y = fmaxf(y, 0.0f);
-                }
-                const uint32_t h = __half_as_ushort(__float2half_rn(y));
-                if constexpr (kNext) {
-                  if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
-                }
-                yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
-                if constexpr (kDebug) pc[j] = acc;
-              }
+              };
+              // the whole group's test picks one form for the slice (a uniform branch)
+              if (kZp && !z32) slice_y(Wide<true>{});
+              else slice_y(Wide<false>{});
               box_reuse_wait(lane);
               box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
                             n0 + j0, lane, y_policy);
@@ -1020,40 +1034,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto emit = [&](int j0, const int (&accv)[kW], const float (&fov)[kW]) {
           const float ra_s = ra[0];  // this slice's tokens, one per lane
           [[maybe_unused]] const int za_s = kZp ? za[0] : 0;
+          // zeropoint: the int32 form is exact for all 32 tokens of the group (uniform)
+          [[maybe_unused]] const bool z32 = kZp && __all_sync(0xffffffffu, abs(za_s) <= p.z_safe);
           uint4 xa, xb;
           cc_load_rows(p, n0 + j0, n_cc, lane, xa, xb);
           float fcc[kW];  // outlier product of this slice (zeros unless cc)
           cc_outlier_slice(n_cc, wh, xa, xb, fcc);
           uint32_t yh[kW / 2];
+          auto slice_y = [&](auto wide) {
   #pragma unroll
-          for (int j = 0; j < kW; ++j) {
-            const int acc = accv[j];
-            const float fo = fov[j] + fcc[j];
-            const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
-            float y;
-            if constexpr (kZp) {
-              // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32 when
-              // |Z| <= z_safe bounds it below 2^31 (token j is the same for the whole warp,
-              // so the branch is uniform), in 64 bits otherwise
-              const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
-              if (abs(zj) <= p.z_safe) {
-                y = (float)(acc + zj * cbin) * (rj * so) + fo + bo;
+            for (int j = 0; j < kW; ++j) {
+              const int acc = accv[j];
+              const float fo = fov[j] + fcc[j];
+              const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+              float y;
+              if constexpr (kZp) {
+                // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32 when
+                // |Z| <= z_safe bounds it below 2^31, in 64 bits otherwise
+                const int zj = __shfl_sync(0xffffffffu, za_s, (j0 % 32) + j);
+                if constexpr (decltype(wide)::value) {
+                  const long long az = (long long)acc + (long long)zj * (long long)cbin;
+                  y = __fmaf_rn(__ll2float_rn(az), rj * so, fo) + bo;
+                } else {
+                  y = __fmaf_rn((float)(acc + zj * cbin), rj * so, fo) + bo;
+                }
               } else {
-                const long long az = (long long)acc + (long long)zj * (long long)cbin;
-                y = __ll2float_rn(az) * (rj * so) + fo + bo;
+                y = __fmaf_rn((float)acc, rj * so, fo) + bo;
               }
-            } else {
-              y = (float)acc * (rj * so) + fo + bo;
+              if constexpr (kNext) {
+                if (p.next_relu) y = fmaxf(y, 0.0f);
+              }
+              const uint32_t h = __half_as_ushort(__float2half_rn(y));
+              if constexpr (kNext) {
+                if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
+              }
+              yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
             }
-            if constexpr (kNext) {
-              if (p.next_relu) y = fmaxf(y, 0.0f);
-            }
-            const uint32_t h = __half_as_ushort(__float2half_rn(y));
-            if constexpr (kNext) {
-              if (n0 + j0 + j < p.T) ymax = max(ymax, h & 0x7fffu);
-            }
-            yh[j / 2] = (j & 1) ? (yh[j / 2] | (h << 16)) : h;
-          }
+          };
+          // the whole group's test picks one form for the slice (a uniform branch)
+          if (kZp && !z32) slice_y(Wide<true>{});
+          else slice_y(Wide<false>{});
           box_reuse_wait(lane);
           box_store<kW>(boxes + slot * C::kBoxBytes, yh, mapY, p.Y, p.T, p.out, m0 + 32 * q,
                         n0 + j0, lane, y_policy);
