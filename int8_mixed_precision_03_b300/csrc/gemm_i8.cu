@@ -153,7 +153,13 @@ struct Cfg {
   static constexpr int b = a16 + (kAT ? 0 : kStages * kA16Bytes);
   static constexpr int a8 = b + kStages * kBStage;
   static constexpr int box = a8 + kStages8 * kA8Slot;
-  static constexpr int bars = box + 4 * 2 * kBoxBytes;
+  // the tile's transposed X_out rows (CUDA-core outlier product, whole-tile schedule), where
+  // they fit: [kCcOut rows][BN tokens] fp16
+  static constexpr int xo = box + 4 * 2 * kBoxBytes;
+  static constexpr int kXoWant = kCcOut * BN * 2;
+  static constexpr int kXoBytes =
+      xo + kXoWant + (3 * kStages + 2 * kStages8 + 6) * 8 + 16 + 1024 <= kMaxSmem ? kXoWant : 0;
+  static constexpr int bars = xo + kXoBytes;
   // full_a, full_b, empty [kStages]; a8_full, a8_empty [kStages8]; tmem_full,
   // tmem_empty [2]; done; epi (the four epilogue warps' rendezvous of split tiles)
   static constexpr int kNumBars = 3 * kStages + 2 * kStages8 + 2 * 2 + 2;
@@ -313,6 +319,36 @@ __device__ __forceinline__ void cc_load_rows(const Params& p, int tok0, int n, i
     const uint4* src = reinterpret_cast<const uint4*>(p.xoT + (size_t)lane * p.xo_stride + tok0);
     a = __ldg(src);
     b = __ldg(src + 1);
+  }
+}
+
+// The same product with the slice's rows read from the tile's staged copy in shared memory
+// (row k of the tile at xo + k * pitch bytes, tokens from the slice's first): every lane
+// reads the same 32 bytes per row (broadcast loads), so no shuffles are needed.
+__device__ __forceinline__ void cc_outlier_slice_smem(int n, const uint32_t (&wh)[kCcOut / 2],
+                                                      uint32_t xo, uint32_t pitch,
+                                                      float (&fo)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) fo[j] = 0.0f;
+#pragma unroll
+  for (int k0 = 0; k0 < kCcOut; k0 += 4) {
+    if (k0 >= n) break;
+    uint4 xa[4], xb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t a = xo + (uint32_t)(k0 + u) * pitch;
+      xa[u] = ld_shared_v4(a);
+      xb[u] = ld_shared_v4(a + 16);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u;
+      const uint32_t w2 = wh[k >> 1];
+      const uint32_t xw[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
+                              xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) fma2_f16_f32(fo[2 * e], fo[2 * e + 1], xw[e], w2, k & 1);
+    }
   }
 }
 
@@ -810,8 +846,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t y_policy = l2_policy_evict_first();
       // this CTA's running-sum slot, [BN tokens][128 features]; lane = feature 32q + lane
       int32_t* accs = p.acc_scratch + (size_t)blockIdx.x * BN * 128 + 32 * q + lane;
-      uint32_t nseg = 0, slot = 0;
+      uint32_t nseg = 0, slot = 0, ephase = 0;
       bool ok = true;
+      // CUDA-core outlier product: the tile's transposed X_out rows are staged once in shared
+      // memory by the four epilogue warps (where they fit), so that each slice reads them
+      // with broadcast loads instead of shuffles
+      constexpr bool kXoSmem = C::kXoBytes > 0;
+      [[maybe_unused]] const uint32_t xo_s = sbase + C::xo;
+      // rendezvous of the four epilogue warps (bounded: an aborted pipeline unwinds)
+      [[maybe_unused]] auto epi_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_bar);
+        const bool r = pipe_wait(epi_bar, ephase & 1u, ab);
+        ++ephase;
+        return r;
+      };
       for (int t = tile_first<kPair>(); t < tiles && ok; t += tile_stride<kPair>()) {
         const int m_blk = t / p.n_tiles, n_blk = t % p.n_tiles;
         const int m0 = m_blk * kFeatTile + (int)rank * BM, n0 = n_blk * BN;
@@ -832,6 +881,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             (kZp && o_ok) ? __ldg(&p.cbsum[o]) - __ldg(&p.cbout[o]) : 0;
         uint32_t wh[kCcOut / 2];  // this feature's outlier weights (CUDA-core outlier product)
         load_cc_weights(p, o, o_ok, n_cc, wh);
+        if constexpr (kXoSmem) {
+          if (n_cc > 0) {
+            // rows 0 .. n_cc rounded up to 4 (zeros past n_cc), the tile's tokens present in
+            // the transposed copy (its rows hold T rounded up to 16), in 16-byte chunks;
+            // the previous tile's rows are no longer read once all four warps arrive
+            if (!(ok = epi_sync())) break;
+            const int rows = (n_cc + 3) & ~3;
+            const int cpr = min(BN, p.xo_stride - n0) / 8;
+            const int et = 32 * q + lane;
+            for (int c = et; c < rows * cpr; c += 128) {
+              const int k = c / cpr, ch = c - k * cpr;
+              const uint4 v =
+                  __ldg(reinterpret_cast<const uint4*>(p.xoT + (size_t)k * p.xo_stride + n0) + ch);
+              st_shared_v4(xo_s + (uint32_t)(k * BN + ch * 8) * 2u, v.x, v.y, v.z, v.w);
+            }
+            if (!(ok = epi_sync())) break;
+          }
+        }
         const int nseg_int = count_int_segments(p, n_blk, 0, p.nchunks);
         const int nseg_tile = nseg_int + (nkb_out > 0 ? 1 : 0);
         uint32_t ymax = 0;  // kNext: largest fp16 magnitude bits of this lane's column
@@ -850,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kW; ++j) pn[j] = first ? 0 : accs[(size_t)j * 128];
           static_assert(kW == 16, "CUDA-core outlier slices are 16 tokens");
           uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;  // the slice's transposed X_out
-          if (last) cc_load_rows(p, n0, n_cc, lane, xa, xb);  // rows (CUDA-core outliers)
+          if (!kXoSmem && last) cc_load_rows(p, n0, n_cc, lane, xa, xb);  // rows (shuffled)
           if (!last) {
             // an int segment that is not the last one of the tile: fold it into the
             // running sum (first segment: store it)
@@ -884,12 +951,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
                 for (int j = 0; j < kW; ++j) pn[j] = accs[(size_t)(j0 + kW + j) * 128];
               }
-              uint4 na, nb;  // the next slice's rows, loaded while this one is computed
-              cc_load_rows(p, n0 + j0 + kW < n0 + BN ? n0 + j0 + kW : p.T, n_cc, lane, na, nb);
               float fcc[kW];  // outlier product of this slice (zeros unless cc)
-              cc_outlier_slice(n_cc, wh, xa, xb, fcc);
-              xa = na;
-              xb = nb;
+              if constexpr (kXoSmem) {
+                cc_outlier_slice_smem(n_cc, wh, xo_s + (uint32_t)j0 * 2u, (uint32_t)BN * 2u, fcc);
+              } else {
+                uint4 na, nb;  // the next slice's rows, loaded while this one is computed
+                cc_load_rows(p, n0 + j0 + kW < n0 + BN ? n0 + j0 + kW : p.T, n_cc, lane, na, nb);
+                cc_outlier_slice(n_cc, wh, xa, xb, fcc);
+                xa = na;
+                xb = nb;
+              }
               uint32_t f[kW];
               tmem_ld<kW>(tF + j0, f);
               tmem_ld_wait();
