@@ -156,7 +156,7 @@ struct Cfg {
   // the tile's transposed X_out rows (CUDA-core outlier product, whole-tile schedule), where
   // they fit: [kCcOut rows][BN tokens] fp16
   static constexpr int xo = box + 4 * 2 * kBoxBytes;
-  static constexpr int kXoWant = kCcOut * BN * 2;
+  static constexpr int kXoWant = kCcOut * BN * 2 + BN * 4;  // + the tile's row scales
   static constexpr int kXoBytes =
       xo + kXoWant + (3 * kStages + 2 * kStages8 + 6) * 8 + 16 + 1024 <= kMaxSmem ? kXoWant : 0;
   static constexpr int bars = xo + kXoBytes;
@@ -852,6 +852,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // memory by the four epilogue warps (where they fit), so that each slice reads them
       // with broadcast loads instead of shuffles
       constexpr bool kXoSmem = C::kXoBytes > 0;
+      // the tile's row scales likewise (their per-token shuffles go too); the zeropoint
+      // epilogue keeps its shuffles, as its zero points would cost registers it lacks
+      constexpr bool kRsSmem = kXoSmem && !kZp;
       [[maybe_unused]] const uint32_t xo_s = sbase + C::xo;
       // rendezvous of the four epilogue warps (bounded: an aborted pipeline unwinds)
       [[maybe_unused]] auto epi_sync = [&]() -> bool {
@@ -882,11 +885,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t wh[kCcOut / 2];  // this feature's outlier weights (CUDA-core outlier product)
         load_cc_weights(p, o, o_ok, n_cc, wh);
         if constexpr (kXoSmem) {
+          // the previous tile's rows and scales are no longer read once all four warps arrive;
+          // then the tile's row scales and (n_cc > 0) its transposed outlier rows
+          if (kRsSmem || n_cc > 0) {
+            if (!(ok = epi_sync())) break;
+          }
+          if constexpr (kRsSmem) {
+            for (int j = 32 * q + lane; j < BN; j += 128) {
+              const int tk = n0 + j;
+              st_shared_f32(xo_s + kCcOut * BN * 2 + 4 * j, tk < p.T ? __ldg(&p.rowabs[tk]) : 0.0f);
+            }
+          }
           if (n_cc > 0) {
             // rows 0 .. n_cc rounded up to 4 (zeros past n_cc), the tile's tokens present in
             // the transposed copy (its rows hold T rounded up to 16), in 16-byte chunks;
             // the previous tile's rows are no longer read once all four warps arrive
-            if (!(ok = epi_sync())) break;
             const int rows = (n_cc + 3) & ~3;
             const int cpr = min(BN, p.xo_stride - n0) / 8;
             const int et = 32 * q + lane;
@@ -896,6 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __ldg(reinterpret_cast<const uint4*>(p.xoT + (size_t)k * p.xo_stride + n0) + ch);
               st_shared_v4(xo_s + (uint32_t)(k * BN + ch * 8) * 2u, v.x, v.y, v.z, v.w);
             }
+          }
+          if (kRsSmem || n_cc > 0) {
             if (!(ok = epi_sync())) break;
           }
         }
@@ -975,6 +990,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               [[maybe_unused]] const bool z32 =
                   kZp && __all_sync(0xffffffffu, abs(za_s) <= p.z_safe);
               uint32_t yh[kW / 2];
+              [[maybe_unused]] uint32_t rsv[kW];  // the slice's row scales (kRsSmem)
+              if constexpr (kRsSmem) {
+  #pragma unroll
+                for (int c = 0; c < kW / 4; ++c) {
+                  const uint4 r4 = ld_shared_v4(xo_s + kCcOut * BN * 2 + 4 * (j0 + 4 * c));
+                  rsv[4 * c] = r4.x;
+                  rsv[4 * c + 1] = r4.y;
+                  rsv[4 * c + 2] = r4.z;
+                  rsv[4 * c + 3] = r4.w;
+                }
+              }
               auto slice_y = [&](auto wide) {
   #pragma unroll
                 for (int j = 0; j < kW; ++j) {
@@ -986,7 +1012,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   } else {
                     acc = __float2int_rn(__uint_as_float(f[j])) + pc[j];
                   }
-                  const float rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
+                  float rj;
+                  if constexpr (kRsSmem) rj = __uint_as_float(rsv[j]);
+                  else rj = __shfl_sync(0xffffffffu, ra_s, (j0 % 32) + j);
                   float y;
                   if constexpr (kZp) {
                     // x ~ (q + Z)/S: sum_j (q_j + Z) CB_j = acc + Z * cbin, exact: in int32
