@@ -41,6 +41,26 @@ def test_absmax_worked_example_from_page():
     assert Q[0].tolist() == expect == [28, -12, -101, 127]
 
 
+def test_int8_weight_footprint_matches_page_memory_example():
+    """The page's 7B example stores the weights in a quarter of their fp32 bytes (the size
+    estimator counts one byte per parameter). The quantized weight format's codes take the
+    same quarter, inside the rounding of the printed sizes; its one fp32 scale per output
+    feature comes on top (4 bytes per row of `in` codes)."""
+    g = json.load(open(os.path.join(GOLDEN, "int8_memory_example.json")))
+    lo = (g["fp32_gb_printed"] - 0.005) / (g["int8_gb_printed"] + 0.005)
+    hi = (g["fp32_gb_printed"] + 0.005) / (g["int8_gb_printed"] - 0.005)
+    assert lo <= g["ratio_printed"] <= hi
+    rng = np.random.default_rng(11)
+    out, d = 256, 4096  # rows of a 7B-class layer (hidden size 4096)
+    W = (rng.standard_normal((out, d)) * 0.02).astype(np.float16)
+    CB, SCB = oracle.quantize_weight(W)
+    assert CB.dtype == np.int8 and CB.shape == (out, d)
+    assert SCB.dtype == np.float32 and SCB.shape == (out,)
+    ratio = (4 * W.size) / CB.nbytes
+    assert lo <= ratio <= hi, ratio
+    assert SCB.nbytes == 4 * out
+
+
 # --------------------------------------------------------------------------- fp16 handling
 def test_half_conversions_match_numpy():
     g = np.random.default_rng(7)
