@@ -41,19 +41,24 @@
 // last of its tile is folded into it, and the tile's last segment reads it back.
 // Outlier product: with at most kCcOut outlier columns (the usual case: about 0.1% of the
 // hidden dimensions) the epilogue computes it on the CUDA cores, sum_k X_out[t,k] W_out[o,k]
-// in fp32 from a token-contiguous transposed copy of X_out (one broadcast load per column
-// and 16 tokens) and this feature's W_out row held in registers. A tile then has no short
+// in fp32 from a token-contiguous transposed copy of X_out and this feature's W_out row
+// held in registers. On the whole-tile schedule the four epilogue warps copy the tile's rows
+// of that copy into shared memory once per tile and each 16-token slice reads them with
+// broadcast loads; on the split schedule lane k loads row k of a slice and shuffles pass it
+// on (shuffles compete with the mainloop's shared-memory traffic). A tile then has no short
 // outlier segment after its long int segment, so the next tile's MMAs never wait for the
 // epilogue to drain the int accumulator. With more outlier columns they run as the tile's
 // last MMA segment (fp16 operands, fp32 accumulation in TMEM) of ceil(n/64) K blocks.
 // Epilogue: Y[t, o] = fp16(acc * rowabs[t] * SCB[o] / 127^2 + outlier + bias[o]), staged
 // per warp in shared memory (two boxes of tokens x 32 features) and written by TMA stores.
+// The tokens' row scales come from a per-tile copy in shared memory on the whole-tile
+// schedule (broadcast loads, four per 16-token slice), from shuffles otherwise.
 // L2 policy: the activation codes, re-read by every weight strip, are loaded evict-last,
 // and Y, written once, is stored evict-first, so that the codes stay in L2 across waves.
 // With zeropoint activation codes (x ~ (q + Z)/S per token, "LLM.int8() summary" (zenn),
 // "Zeropoint Quantization") the epilogue adds Z_t times the feature's code sum over the
-// inlier columns to the exact int32 product, in 64-bit integers, before scaling by
-// rowabs = 127/S.
+// inlier columns to the exact int32 product before scaling by rowabs = 127/S: in int32
+// when |Z| is small enough for every token of a 32-token group, in 64 bits otherwise.
 // When Y is the input of a following int8 matmul (an FFN's up projection), the epilogue
 // also applies the activation (ReLU or none) and computes that matmul's outlier flags:
 // each lane owns one column of Y, keeps the largest fp16 magnitude over the tile's valid
