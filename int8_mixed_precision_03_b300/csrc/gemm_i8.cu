@@ -903,8 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (n_cc > 0) {
             // rows 0 .. n_cc rounded up to 4 (zeros past n_cc), the tile's tokens present in
-            // the transposed copy (its rows hold T rounded up to 16), in 16-byte chunks;
-            // the previous tile's rows are no longer read once all four warps arrive
+            // the transposed copy (its rows hold T rounded up to 16), in 16-byte chunks
             const int rows = (n_cc + 3) & ~3;
             const int cpr = min(BN, p.xo_stride - n0) / 8;
             const int et = 32 * q + lane;
