@@ -271,6 +271,25 @@ def test_zeropoint_uses_full_range_on_one_sided_rows():
     assert (np.abs(rec - Xf)[interior] <= (step * 0.5001 + 1e-7)[np.nonzero(interior)[0], 0]).all()
 
 
+def test_absmax_leaves_the_negative_codes_unused_on_relu_rows():
+    """zenn summary, "Zeropoint Quantization": on ReLU outputs absmax codes use only half of
+    [-127, 127] (the negative half is wasted), which zeropoint codes recover. On the same
+    one-sided rows the absmax codes lie in [0, 127] with 127 reached, while the zeropoint
+    codes reach both ends; the zeropoint step is therefore about half the absmax step."""
+    w = synth.WORKLOADS["tiny"].with_(T=8, d_in=512)
+    X = synth.make_relu_like(w)
+    X[:, ::7] = 0  # ReLU zeros
+    Xf = X.astype(np.float64)
+    assert (Xf >= 0).all() and (Xf.min(1) == 0).all()
+    Qa, a = oracle.quantize_rows_absmax(X)
+    assert (Qa.min(1) >= 0).all() and (Qa.max(1) == 127).all()
+    Qz, S, Z = oracle.zeropoint_rows(X)
+    assert (Qz.min(1) == -127).all() and (Qz.max(1) == 127).all()
+    step_abs = a.astype(np.float64) / 127.0
+    step_zp = 1.0 / S.astype(np.float64)
+    np.testing.assert_allclose(step_zp / step_abs, 127.0 / 254.0, rtol=1e-6)
+
+
 def test_zeropoint_zero_maps_exactly_and_constant_row():
     X = np.array([[0.0, 1.5, -2.0, 0.25, 0.0, 3.0],
                   [2.5, 2.5, 2.5, 2.5, 2.5, 2.5]], np.float16)
